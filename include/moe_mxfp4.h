@@ -1,0 +1,210 @@
+/*
+ * moe_mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 routed-expert MoE layer.
+ *
+ * One MoE layer forward is six stream-ordered calls:
+ *
+ *   moe_route_topk           router logits + top-k + routing weights
+ *   moe_sort_tokens          group the token->expert assignments by expert
+ *   act_quant_q8             Q8 (int8 per 32 + fp32 scale) of the activations
+ *   moe_mxfp4_gateup_swiglu  h = silu(Wg x) * (Wu x) per assignment (MXFP4 weights)
+ *   act_quant_q8             Q8 of h
+ *   moe_mxfp4_down           y = Wd h per assignment
+ *   moe_combine              out[t] = sum_j w[t,j] * y[t*k+j], slot order
+ *
+ * It follows the layer as the DeepSeek-V4-Flash pages describe it:
+ *  - "DeepSeek-V4-Flash on AMD gfx90a: Correctness Recovery and Inference
+ *    Performance Engineering": Fig. 1 (router top-6 -> routed experts gate/up ->
+ *    down -> add partials), §6.1 (packed 4-bit FP4 weights, online INT8 per-32
+ *    activation quantisation, E2M1 nibbles as 0,±1,..,±12, integer dot then
+ *    activation and E8M0 scaling), §7.1 item 8 (expert sorter), §8.2 (FP32 top-k
+ *    partials and a fixed reduction), §5.3 (deterministic top-k ties by logical id);
+ *  - "Optimizing DeepSeek V4 Flash Inference on a Strix Halo Pair": "MXFP4
+ *    routed-expert kernels" and "The exact-rows contract" (one weight pass
+ *    serves K resident rows; every row keeps the one-row arithmetic; explicit
+ *    output strides);
+ *  - "feat(ds4): add concurrent serving on Strix Halo and R9700 + Strix":
+ *    "Reduce expert-route overhead" (negative sentinels for unowned slots).
+ *
+ * Conventions shared by every call
+ *  - All pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or retains them, and never synchronises the stream.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work; results are ready when the stream reaches them.
+ *  - Matrices are row-major; ld_* are row strides in ELEMENTS of that array.
+ *  - Validation of sizes, strides, alignment and null pointers happens on the
+ *    host before any launch; a failing call enqueues nothing and returns
+ *    MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED), with the reason in
+ *    moe_last_error().  Launch failures return MOE_ERR_CUDA.
+ *  - Values the host cannot see (expert ids, sort offsets) are bounds-checked
+ *    on the device; an out-of-range value is skipped and raises a bit in the
+ *    device status word, read by moe_device_status().
+ *  - Deterministic: no floating-point atomics.  Every row's result is computed
+ *    by the same arithmetic whatever the number of rows T in the call, so a
+ *    T-row call gives, row by row, the bits of T one-row calls.
+ *  - Requires an sm_103a device (GB300); MOE_ERR_UNSUPPORTED otherwise.
+ *
+ * Weight layout (one layer; E experts; all contiguous, 16-byte aligned):
+ *  - wg, wu: uint8 [E][I][H/2]; byte c of a row holds element 2c in its low
+ *    nibble and 2c+1 in its high nibble; a nibble is an E2M1 code (OCP MX).
+ *  - sg, su: uint8 [E][I][H/32]; one E8M0 byte (2^(u-127); 255 = NaN) per 32
+ *    consecutive elements of a row.
+ *  - wd: uint8 [E][H][I/2], sd: uint8 [E][H][I/32], same conventions.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported from libmoe_mxfp4.so (everything else in it is hidden). */
+#ifndef MOE_API
+#define MOE_API __attribute__((visibility("default")))
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* bad size, stride, alignment or null pointer; nothing enqueued */
+    MOE_ERR_UNSUPPORTED = 2, /* shape or device outside what this build handles */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE = 4       /* moe_device_status: the device status word was non-zero */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Device status bits (moe_device_status). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1u  /* an expert id outside [0, E) was skipped */
+#define MOE_DEV_BAD_ROW 0x2u        /* a sorted entry or offset outside its range was skipped */
+#define MOE_DEV_WAIT_TIMEOUT 0x4u   /* a bounded wait on a copy gave up; outputs are incomplete */
+
+/* Message for the last non-OK status returned on this host thread. */
+MOE_API const char *moe_last_error(void);
+
+/* ABI version of this header (bumped on any signature change). */
+MOE_API int moe_abi_version(void);
+#define MOE_ABI_VERSION 1
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device into *flags (may be NULL).  Returns MOE_ERR_DEVICE when the
+ * word was non-zero.  Test and debugging aid; not for the hot path. */
+MOE_API moe_status moe_device_status(void *stream, uint32_t *flags);
+
+/* ---------------------------------------------------------------- routing */
+
+/* Router and top-k.  Fig. 1 of the gfx90a report ("Router Top-6"), with §5.3's
+ * deterministic selection.
+ *  x        [T][ld_x] activations (MOE_F32 or MOE_BF16), first H columns used.
+ *  w_router [E][H] router weights (MOE_F32 or MOE_BF16).
+ *  bias     [E] fp32 logit bias, or NULL.
+ *  logits   [T][E] fp32 output: the router logits (no bias), each the fp32
+ *           result of one fixed summation order -- H is cut into chunks of 8
+ *           consecutive elements, chunk c feeds partial sum c mod 32 (chunks in
+ *           increasing order, one fused multiply-add per element), then the 32
+ *           partials are added pairwise p[l] += p[l+s], s = 16, 8, 4, 2, 1.
+ *  ids      [T][k] int32 output: the k experts of largest score = logit + bias,
+ *           ties to the lower id, in descending score order.
+ *  weights  [T][k] fp32 output: sigmoid(score) renormalised over the k slots.
+ * Requires H % 8 == 0, 1 <= k <= min(E, 8), E <= 1024; x and w_router
+ * 16-byte aligned, ld_x * element size a multiple of 16 bytes. */
+MOE_API moe_status moe_route_topk(const void *x, moe_dtype x_dtype, int64_t ld_x,
+                          const void *w_router, moe_dtype w_dtype, const float *bias,
+                          int T, int H, int E, int k,
+                          float *logits, int32_t *ids, float *weights, void *stream);
+
+/* ---------------------------------------------------------------- sorter */
+
+/* Length the `sorted` array needs: T*k + E*(tile_rows-1). */
+MOE_API int64_t moe_sort_tokens_capacity(int T, int k, int E, int tile_rows);
+
+/* Stable counting sort of the A = T*k assignments a = t*k + j by expert (the
+ * expert sorter of the gfx90a report, §7.1 item 8).
+ *  ids      [T][k] expert ids.
+ *  offsets  [E+1] output: expert e owns sorted[offsets[e] .. offsets[e+1]).
+ *  sorted   [cap] output: assignment ids, increasing within each expert; each
+ *           expert's segment is padded to a multiple of tile_rows with -1
+ *           (the negative sentinel of the lucebox PR, "Reduce expert-route
+ *           overhead").  Entries past offsets[E] are not written.
+ *  inv      [T*k] output: position of assignment a in `sorted` (-1 if its id
+ *           was out of range).
+ * Requires E <= 1024, tile_rows >= 1, cap >= moe_sort_tokens_capacity(). */
+MOE_API moe_status moe_sort_tokens(const int32_t *ids, int T, int k, int E, int tile_rows,
+                           int32_t *offsets, int32_t *sorted, int64_t cap, int32_t *inv,
+                           void *stream);
+
+/* ---------------------------------------------------------------- Q8 */
+
+/* Q8 quantisation, per row and per block of 32 columns (the gfx90a report,
+ * §6.1 "online BF16 activation quantization to INT8 per 32 elements"):
+ * amax = max|x|, scale = amax/127 (IEEE fp32 division), q = round-to-nearest-
+ * even(x * (1/scale)) clamped to [-127, 127]; amax = 0 gives scale 0, q = 0.
+ *  x      [rows][ld_x] MOE_F32 or MOE_BF16 (finite values).
+ *  q      [rows][ld_q] int8 output;  scale [rows][ld_s] fp32 output.
+ * Requires cols % 32 == 0; x and q 16-byte aligned with row strides that are
+ * multiples of 16 bytes. */
+MOE_API moe_status act_quant_q8(const void *x, moe_dtype x_dtype, int rows, int cols, int64_t ld_x,
+                        int8_t *q, int64_t ld_q, float *scale, int64_t ld_s, void *stream);
+
+/* ---------------------------------------------------------------- experts */
+
+/* Gate/up MXFP4 projections with SwiGLU (the Strix Halo record, "MXFP4
+ * routed-expert kernels": register-resident gate/up reductions; the lucebox PR
+ * folds SwiGLU into the gate/up pass).  For every assignment a in `sorted`
+ * (entries < 0 skipped) with expert e = the segment it sits in, token t = a/k:
+ *   G[i] = sum_b I_b * xs[t,b] * 2^(sg[e,i,b]-128), U[i] likewise,
+ *   I_b  = exact integer sum over the 32 elements of block b of
+ *          xq[t,.] * (2 * E2M1 value)  (twice the E2M1 value is an integer),
+ *   h[a, i] = silu(G[i]) * U[i],   silu(g) = g / (1 + exp(-g)).
+ * Scaled block terms are accumulated in fp32 in a fixed order independent of
+ * the number of rows.  One pass over an expert's weights serves all its rows.
+ *  xq [T][ld_xq] int8, xs [T][ld_xs] fp32  (Q8 of the activations).
+ *  offsets [E+1], sorted [cap] from moe_sort_tokens.
+ *  h [T*k][ld_h] fp32 output; rows of assignments not in `sorted` untouched.
+ * Requires H % 128 == 0, H <= 4096, I % 128 == 0; xq 16-byte aligned, ld_xq a
+ * multiple of 16; weights 16-byte aligned. */
+MOE_API moe_status moe_mxfp4_gateup_swiglu(const int8_t *xq, int64_t ld_xq, const float *xs, int64_t ld_xs,
+                                   const uint8_t *wg, const uint8_t *sg,
+                                   const uint8_t *wu, const uint8_t *su,
+                                   const int32_t *offsets, const int32_t *sorted, int64_t cap,
+                                   int T, int k, int E, int H, int I,
+                                   float *h, int64_t ld_h, void *stream);
+
+/* The same projections without the activation: g[a,i] = G[i], u[a,i] = U[i]
+ * (same arithmetic, same bits as the values silu() is applied to above).
+ * g and u are [T*k][ld_gu] fp32 outputs. */
+MOE_API moe_status moe_mxfp4_gateup(const int8_t *xq, int64_t ld_xq, const float *xs, int64_t ld_xs,
+                            const uint8_t *wg, const uint8_t *sg,
+                            const uint8_t *wu, const uint8_t *su,
+                            const int32_t *offsets, const int32_t *sorted, int64_t cap,
+                            int T, int k, int E, int H, int I,
+                            float *g, float *u, int64_t ld_gu, void *stream);
+
+/* Down MXFP4 projection (the gfx90a report, §6.1 "top-6 slots in the down
+ * projection", §8.2 FP32 top-k partials): for every assignment a in `sorted`
+ * with expert e, y[a, n] = sum_b I_b * hs[a,b] * 2^(sd[e,n,b]-128), n < H,
+ * same block dot and fixed fp32 order as above.
+ *  hq [T*k][ld_hq] int8, hs [T*k][ld_hs] fp32 (Q8 of h).
+ *  y  [T*k][ld_y] fp32 output.
+ * Requires I % 128 == 0, I <= 4096, H % 128 == 0; hq 16-byte aligned, ld_hq a
+ * multiple of 16; weights 16-byte aligned. */
+MOE_API moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *hs, int64_t ld_hs,
+                          const uint8_t *wd, const uint8_t *sd,
+                          const int32_t *offsets, const int32_t *sorted, int64_t cap,
+                          int T, int k, int E, int H, int I,
+                          float *y, int64_t ld_y, void *stream);
+
+/* ---------------------------------------------------------------- combine */
+
+/* Routing-weighted combine in slot order (the gfx90a report, §8.2 "FP32 top-k
+ * partial and fixed reduction"): out[t,n] = fma(w[t,k-1], y[t*k+k-1,n], ...
+ * fma(w[t,1], y[t*k+1,n], w[t,0]*y[t*k,n])), fp32.
+ *  y [T*k][ld_y], w [T][k] fp32; out [T][ld_out] fp32 output. */
+MOE_API moe_status moe_combine(const float *y, int64_t ld_y, const float *w, int T, int k, int H,
+                       float *out, int64_t ld_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXFP4_H */

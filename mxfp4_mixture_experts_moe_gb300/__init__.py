@@ -1,0 +1,181 @@
+"""GB300 (sm_103a) MXFP4 routed-expert MoE layer: thin Python binding.
+
+Every function here only marshals torch tensors into the C ABI of
+``libmoe_mxfp4.so`` (declared in ``include/moe_mxfp4.h``) and raises on a
+non-OK status.  All arithmetic runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback: the first call fails loudly when the library has not
+been built (``python -m mxfp4_mixture_experts_moe_gb300.build``).
+
+The functions keep the C names and argument order, minus the sizes, which are
+read from the tensors' shapes, and with the stream defaulting to PyTorch's
+current stream.  The library is loaded on first use (so that the build
+module can be imported before it exists); a missing library raises there.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+
+EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
+           "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
+           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine"]
+
+_P, _I, _L = C.c_void_p, C.c_int, C.c_int64
+_SIG = {
+    "moe_last_error": (C.c_char_p, []),
+    "moe_abi_version": (_I, []),
+    "moe_device_status": (_I, [_P, C.POINTER(C.c_uint32)]),
+    "moe_route_topk": (_I, [_P, _I, _L, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_sort_tokens_capacity": (_L, [_I, _I, _I, _I]),
+    "moe_sort_tokens": (_I, [_P, _I, _I, _I, _I, _P, _P, _L, _P, _P]),
+    "act_quant_q8": (_I, [_P, _I, _I, _I, _L, _P, _L, _P, _L, _P]),
+    "moe_mxfp4_gateup_swiglu": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _L, _P]),
+    "moe_mxfp4_gateup": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _P, _L, _P]),
+    "moe_mxfp4_down": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _L, _P]),
+    "moe_combine": (_I, [_P, _L, _P, _I, _I, _I, _P, _L, _P]),
+}
+library_path = _LIB_PATH
+
+
+class _Native:
+    """The loaded C library; loads on first attribute access, raises if absent."""
+    _cdll = None
+
+    def __getattr__(self, name):
+        if _Native._cdll is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                                  "`python -m mxfp4_mixture_experts_moe_gb300.build` (there is no fallback path)")
+            lib = C.CDLL(_LIB_PATH)
+            for fname, (res, args) in _SIG.items():
+                f = getattr(lib, fname)
+                f.restype = res
+                f.argtypes = args
+            _Native._cdll = lib
+        return getattr(_Native._cdll, name)
+
+
+_lib = _Native()
+
+
+def load():
+    """Load the library now (raises ImportError if it has not been built)."""
+    _lib.moe_abi_version
+    return _Native._cdll
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, _lib.moe_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ld(t):
+    assert t.dim() == 2 and t.stride(1) == 1, "expected a 2-D tensor with unit column stride"
+    return t.stride(0)
+
+
+def moe_abi_version() -> int:
+    return _lib.moe_abi_version()
+
+
+def moe_last_error() -> str:
+    return _lib.moe_last_error().decode(errors="replace")
+
+
+def moe_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status bits."""
+    flags = C.c_uint32(0)
+    st = _lib.moe_device_status(_stream(stream), C.byref(flags))
+    if st not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(st)
+    return flags.value
+
+
+def moe_route_topk(x, w_router, bias, k, logits, ids, weights, stream=None):
+    T, H = x.shape[0], w_router.shape[1]
+    E = w_router.shape[0]
+    _check(_lib.moe_route_topk(_ptr(x), _dt(x), _ld(x), _ptr(w_router), _dt(w_router), _ptr(bias),
+                               T, H, E, k, _ptr(logits), _ptr(ids), _ptr(weights), _stream(stream)))
+
+
+def moe_sort_tokens_capacity(T, k, E, tile_rows=1) -> int:
+    return _lib.moe_sort_tokens_capacity(T, k, E, tile_rows)
+
+
+def moe_sort_tokens(ids, E, tile_rows, offsets, sorted_, inv, stream=None):
+    T, k = ids.shape
+    _check(_lib.moe_sort_tokens(_ptr(ids), T, k, E, tile_rows, _ptr(offsets), _ptr(sorted_),
+                                sorted_.numel(), _ptr(inv), _stream(stream)))
+
+
+def act_quant_q8(x, q, scale, stream=None):
+    rows, cols = x.shape
+    _check(_lib.act_quant_q8(_ptr(x), _dt(x), rows, cols, _ld(x), _ptr(q), _ld(q), _ptr(scale), _ld(scale),
+                             _stream(stream)))
+
+
+def moe_mxfp4_gateup_swiglu(xq, xs, wg, sg, wu, su, offsets, sorted_, k, h, stream=None):
+    T, H = xq.shape[0], wg.shape[2] * 2
+    E, I = wg.shape[0], wg.shape[1]
+    _check(_lib.moe_mxfp4_gateup_swiglu(_ptr(xq), _ld(xq), _ptr(xs), _ld(xs), _ptr(wg), _ptr(sg), _ptr(wu),
+                                        _ptr(su), _ptr(offsets), _ptr(sorted_), sorted_.numel(), T, k, E, H, I,
+                                        _ptr(h), _ld(h), _stream(stream)))
+
+
+def moe_mxfp4_gateup(xq, xs, wg, sg, wu, su, offsets, sorted_, k, g, u, stream=None):
+    T, H = xq.shape[0], wg.shape[2] * 2
+    E, I = wg.shape[0], wg.shape[1]
+    assert g.stride() == u.stride()
+    _check(_lib.moe_mxfp4_gateup(_ptr(xq), _ld(xq), _ptr(xs), _ld(xs), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su),
+                                 _ptr(offsets), _ptr(sorted_), sorted_.numel(), T, k, E, H, I, _ptr(g), _ptr(u),
+                                 _ld(g), _stream(stream)))
+
+
+def moe_mxfp4_down(hq, hs, wd, sd, offsets, sorted_, T, k, y, stream=None):
+    E, H, I = wd.shape[0], wd.shape[1], wd.shape[2] * 2
+    _check(_lib.moe_mxfp4_down(_ptr(hq), _ld(hq), _ptr(hs), _ld(hs), _ptr(wd), _ptr(sd), _ptr(offsets),
+                               _ptr(sorted_), sorted_.numel(), T, k, E, H, I, _ptr(y), _ld(y), _stream(stream)))
+
+
+def moe_combine(y, w, out, stream=None):
+    T, k = w.shape
+    H = out.shape[1]
+    _check(_lib.moe_combine(_ptr(y), _ld(y), _ptr(w), T, k, H, _ptr(out), _ld(out), _stream(stream)))
+
+
+from .layer import MoeLayer, LayerWeights, Workspace  # noqa: E402

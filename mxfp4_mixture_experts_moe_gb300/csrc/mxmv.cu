@@ -1,0 +1,359 @@
+// MXFP4 expert projections against Q8 activations: gate/up (+SwiGLU) and down.
+//
+// Follows the decode route of "DeepSeek-V4-Flash on AMD gfx90a", §6.1: packed
+// 4-bit weights read without any offline expansion, E2M1 nibbles turned into
+// the small integers 0, ±1, ±2, ±3, ±4, ±6, ±8, ±12, an exact integer dot per
+// block of 32, then activation and E8M0 scaling; and "Optimizing DeepSeek V4
+// Flash Inference on a Strix Halo Pair", "MXFP4 routed-expert kernels" and
+// "The exact-rows contract": one weight pass serves every resident row of an
+// expert and every row keeps the one-row arithmetic.
+//
+// Work split (GB300-first): the grid is one persistent CTA per SM.  CTA c owns
+// the same contiguous slice of output rows [n0, n1) of EVERY expert that has
+// assignments, so the bytes each SM streams are equal whatever the routing.
+// A producer warp streams the CTA's slice of each active expert, one expert
+// per stage, into a ring of shared-memory stages with cp.async.bulk (TMA) for
+// the packed weights and cp.async for the E8M0 bytes, completing on mbarriers.
+// Consumer warps take one output row at a time: lane l owns the 16-byte
+// blocks l, l+32, ... of the row (exactly one MX block each), converts the
+// nibbles once, then loops over the expert's rows.
+//
+// Per row and output, the arithmetic is fixed: lane l accumulates its blocks
+// in increasing order, acc = fma(float(I_b), xs_b * 2^(u_b-128), acc); the 32
+// lane sums are combined by a fixed xor butterfly.  Nothing depends on how
+// many rows the call has, so a T-row call reproduces T one-row calls bit for
+// bit.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+enum Mode { kGateUpSwiglu = 0, kGateUpRaw = 1, kDown = 2 };
+
+struct MxArgs {
+  const int8_t *aq;  // Q8 activation codes: x rows (gate/up, by token) or h rows (down, by assignment)
+  int64_t ld_aq;
+  const float *as;   // Q8 scales
+  int64_t ld_as;
+  const uint8_t *w0, *s0;  // gate (or down) weights / E8M0 bytes, [E][N][K/2] / [E][N][K/32]
+  const uint8_t *w1, *s1;  // up weights / bytes (gate/up only)
+  const int32_t *offsets;  // [E+1]
+  const int32_t *sorted;   // [cap]
+  int64_t cap;
+  int A, k, E;
+  int K;  // reduction length
+  int N;  // output rows per expert
+  float *out0, *out1;
+  int64_t ld_out;
+  int R;              // output rows per CTA (max)
+  int nstage;
+  uint32_t stage_bytes;
+  uint32_t wreg;      // bytes of one matrix's weight slice region in a stage
+  uint32_t sreg;      // bytes of one matrix's scale slice region (16-aligned)
+  int scale16;        // scale rows are whole 16-byte chunks at 16-byte aligned addresses
+  unsigned *status;
+};
+
+MOE_DEVFN float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+template <int MODE, int S>
+__global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
+  constexpr int NM = (MODE == kDown) ? 1 : 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int n_active;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ncons = (blockDim.x >> 5) - 1;
+  const int n0 = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
+  const int n1 = (int)((int64_t)(blockIdx.x + 1) * p.N / gridDim.x);
+  const int R = n1 - n0;
+  const int nb = p.K / 32;
+  const int nstage = p.nstage;
+
+  uint8_t *stages = smem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)nstage * p.stage_bytes);
+  uint64_t *empty = full + nstage;
+  int *active = reinterpret_cast<int *>(empty + nstage);  // [E] active experts, in id order
+  int *offs = active + p.E;                               // [E+1] copy of offsets
+
+  // Stage the expert offsets in one parallel pass, then list the experts
+  // that own rows (ballot compaction keeps increasing id order).
+  for (int i = tid; i <= p.E; i += blockDim.x) offs[i] = p.offsets[i];
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
+      mbar_init(smem_addr(&empty[s]), ncons);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int cnt = 0;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      bool act = false;
+      if (e < p.E) {
+        const int64_t b = offs[e], en = offs[e + 1];
+        const bool bad = b < 0 || en < b || en > p.cap;
+        if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+        act = !bad && en > b;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, act);
+      if (act) active[cnt + __popc(m & lt)] = e;
+      cnt += __popc(m);
+    }
+    if (lane == 0) n_active = cnt;
+  }
+  __syncthreads();
+  const int nact = n_active;
+
+  if (warp == ncons) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    const uint32_t wbytes = (uint32_t)R * (p.K / 2);
+    const uint32_t sbytes = (uint32_t)R * nb;
+    const bool s16 = p.scale16 != 0;
+    int issued = 0;
+    for (int it = 0; it < nact; ++it) {
+      const int st = it % nstage;
+      if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
+      const int e = active[it];
+      const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
+      const uint32_t fb = smem_addr(&full[st]);
+      const int64_t row0 = (int64_t)e * p.N + n0;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, NM * wbytes);
+        bulk_g2s(sbase, p.w0 + row0 * (p.K / 2), wbytes, fb, pol);
+        if (NM == 2) bulk_g2s(sbase + p.wreg, p.w1 + row0 * (p.K / 2), wbytes, fb, pol);
+      }
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        const uint8_t *src = (m == 0 ? p.s0 : p.s1) + row0 * nb;
+        const uint32_t dst = sbase + NM * p.wreg + m * p.sreg;
+        if (s16) {
+          for (uint32_t c = lane; c < sbytes / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+        } else {
+          for (uint32_t c = lane; c < sbytes / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+        }
+      }
+      cp_async_mbar_arrive_noinc(fb);
+      issued = it + 1;
+    }
+    // Never leave with copies in flight into this CTA's shared memory.
+    for (int it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
+      mbar_wait(smem_addr(&full[it % nstage]), (it / nstage) & 1, p.status);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  for (int it = 0; it < nact; ++it) {
+    const int st = it % nstage;
+    if (!mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status)) break;
+    const int e = active[it];
+    const int seg_b = offs[e], seg_e = offs[e + 1];
+    const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
+
+    for (int r = warp; r < R; r += ncons) {
+      uint32_t wq[NM][S][8];
+      float ws[NM][S];
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          const int b = lane + 32 * s;
+          if (b < nb) {
+            const uint4 raw = lds128(sbase + m * p.wreg + (uint32_t)r * (p.K / 2) + 16u * b);
+            e2m1x8_to_off12(raw.x, wq[m][s][0], wq[m][s][1]);
+            e2m1x8_to_off12(raw.y, wq[m][s][2], wq[m][s][3]);
+            e2m1x8_to_off12(raw.z, wq[m][s][4], wq[m][s][5]);
+            e2m1x8_to_off12(raw.w, wq[m][s][6], wq[m][s][7]);
+            ws[m][s] = e8m0_half(lds_u8(sbase + NM * p.wreg + m * p.sreg + (uint32_t)r * nb + b));
+          }
+        }
+      }
+      const int n = n0 + r;
+#pragma unroll 1
+      for (int q = seg_b; q < seg_e; ++q) {
+        const int a = p.sorted[q];
+        if (a < 0) continue;
+        if (a >= p.A) {
+          if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+          continue;
+        }
+        const int64_t arow = (MODE == kDown) ? a : a / p.k;
+        const int8_t *xr = p.aq + arow * p.ld_aq;
+        const float *sr = p.as + arow * p.ld_as;
+        float acc[NM];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          const int b = lane + 32 * s;
+          if (b < nb) {
+            const uint4 x0 = ldg_nc(xr + 32 * b), x1 = ldg_nc(xr + 32 * b + 16);
+            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float sx = sr[b];
+            int xsum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xsum = __dp4a((int)xw[j], 0x01010101, xsum);
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              int d = 0;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) d = __dp4a((int)xw[j], (int)wq[m][s][j], d);
+              const int I = d - 12 * xsum;
+              acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, ws[m][s]), acc[m]);
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xffffffffu, acc[m], o));
+        }
+        if (lane == 0) {
+          float *dst = p.out0 + (int64_t)a * p.ld_out + n;
+          if (MODE == kGateUpSwiglu) *dst = __fmul_rn(silu(acc[0]), acc[NM - 1]);
+          else *dst = acc[0];
+          if (MODE == kGateUpRaw) p.out1[(int64_t)a * p.ld_out + n] = acc[NM - 1];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+  }
+}
+
+template <int MODE>
+moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
+  constexpr int NM = (MODE == kDown) ? 1 : 2;
+  const int nb = p.K / 32;
+  const int S = (nb + 31) / 32;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, name);
+  int smem_optin = 0;
+  err = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return cuda_fail(err, name);
+  const int sms = sm_count();
+  const size_t extra = (size_t)p.E * 8 + 4 + 16 * 8 + 256;
+  int G = p.N < sms ? p.N : sms;
+  for (;;) {
+    p.R = (p.N + G - 1) / G;
+    p.wreg = (uint32_t)p.R * (p.K / 2);
+    p.sreg = ((uint32_t)p.R * nb + 15u) & ~15u;
+    p.stage_bytes = (NM * (p.wreg + p.sreg) + 127u) & ~127u;
+    const size_t avail = (size_t)smem_optin - 1024 - extra;
+    int ns = (int)(avail / p.stage_bytes);
+    if (ns > 8) ns = 8;
+    if (ns >= 2 || G >= p.N) {
+      p.nstage = ns;
+      break;
+    }
+    G = (2 * G < p.N) ? 2 * G : p.N;
+  }
+  if (p.nstage < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
+  p.scale16 = (nb % 16) == 0 && (uintptr_t)p.s0 % 16 == 0 && (p.s1 == nullptr || (uintptr_t)p.s1 % 16 == 0);
+  int per_warp = (p.R + 14) / 15;
+  int ncons = (p.R + per_warp - 1) / per_warp;
+  const size_t smem = (size_t)p.nstage * p.stage_bytes + 2 * 8 * (size_t)p.nstage + (size_t)p.E * 8 + 4;
+  const dim3 block((ncons + 1) * 32);
+
+  static bool configured[3][3][64] = {};
+  const int si = S == 1 ? 0 : (S == 2 ? 1 : 2);
+  auto kern = S == 1 ? mx_expert_kernel<MODE, 1> : (S == 2 ? mx_expert_kernel<MODE, 2> : mx_expert_kernel<MODE, 4>);
+  if (dev < 64 && !configured[MODE][si][dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin - 1024);
+    if (err != cudaSuccess) return cuda_fail(err, name);
+    configured[MODE][si][dev] = true;
+  }
+  kern<<<G, block, smem, stream>>>(p);
+  err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
+}
+
+moe_status check_common(const char *name, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
+                        const void *w0, const void *s0, const void *w1, const void *s1, const int32_t *offsets,
+                        const int32_t *sorted, int64_t cap, int T, int k, int E, int H, int I, const void *out,
+                        int64_t ld_out, int Kred, int rows_act) {
+  if (T < 0 || k <= 0 || E <= 0 || H <= 0 || I <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: T=%d k=%d E=%d H=%d I=%d", name, T, k, E, H, I);
+  if (H % 128 || I % 128) return fail(MOE_ERR_INVALID_ARG, "%s: H=%d and I=%d must be multiples of 128", name, H, I);
+  if (Kred > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: reduction length %d > 4096", name, Kred);
+  if (E > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d > 4096", name, E);
+  if ((int64_t)T * k > 0x7fffffff) return fail(MOE_ERR_UNSUPPORTED, "%s: too many assignments", name);
+  if (T == 0) return MOE_OK;
+  if (!aq || !as || !w0 || !s0 || (w1 == nullptr) != (s1 == nullptr) || !offsets || !sorted || !out)
+    return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if ((uintptr_t)aq % 16 || ld_aq % 16 || ld_aq < Kred) return fail(MOE_ERR_INVALID_ARG, "%s: Q8 codes must be 16-byte aligned with ld a multiple of 16 >= %d (ld=%lld)", name, Kred, (long long)ld_aq);
+  if ((uintptr_t)as % 4 || ld_as < Kred / 32) return fail(MOE_ERR_INVALID_ARG, "%s: bad Q8 scale stride %lld", name, (long long)ld_as);
+  if ((uintptr_t)w0 % 16 || (w1 && (uintptr_t)w1 % 16)) return fail(MOE_ERR_INVALID_ARG, "%s: weights must be 16-byte aligned", name);
+  if ((uintptr_t)s0 % 4 || (s1 && (uintptr_t)s1 % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: scale bytes must be 4-byte aligned", name);
+  if (cap < 0) return fail(MOE_ERR_INVALID_ARG, "%s: cap=%lld", name, (long long)cap);
+  if ((uintptr_t)out % 4) return fail(MOE_ERR_INVALID_ARG, "%s: output must be 4-byte aligned", name);
+  (void)rows_act;
+  (void)ld_out;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const float *xs, int64_t ld_xs,
+                              const uint8_t *wg, const uint8_t *sg, const uint8_t *wu, const uint8_t *su,
+                              const int32_t *offsets, const int32_t *sorted, int64_t cap, int T, int k, int E,
+                              int H, int I, float *o0, float *o1, int64_t ld, void *stream, const char *name) {
+  moe_status st = check_common(name, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T, k, E, H, I, o0,
+                               ld, H, T);
+  if (st != MOE_OK || T == 0) return st;
+  if (!wu) return fail(MOE_ERR_INVALID_ARG, "%s: null up weights", name);
+  if (ld < I) return fail(MOE_ERR_INVALID_ARG, "%s: output ld=%lld < I=%d", name, (long long)ld, I);
+  if (mode == kGateUpRaw && (!o1 || (uintptr_t)o1 % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: bad up output", name);
+  MxArgs p{};
+  p.aq = xq; p.ld_aq = ld_xq; p.as = xs; p.ld_as = ld_xs;
+  p.w0 = wg; p.s0 = sg; p.w1 = wu; p.s1 = su;
+  p.offsets = offsets; p.sorted = sorted; p.cap = cap;
+  p.A = T * k; p.k = k; p.E = E; p.K = H; p.N = I;
+  p.out0 = o0; p.out1 = o1; p.ld_out = ld;
+  p.status = device_status_word();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return mode == kGateUpSwiglu ? launch_mx<kGateUpSwiglu>(p, s, name) : launch_mx<kGateUpRaw>(p, s, name);
+}
+
+extern "C" moe_status moe_mxfp4_gateup_swiglu(const int8_t *xq, int64_t ld_xq, const float *xs, int64_t ld_xs,
+                                              const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
+                                              const uint8_t *su, const int32_t *offsets, const int32_t *sorted,
+                                              int64_t cap, int T, int k, int E, int H, int I, float *h,
+                                              int64_t ld_h, void *stream) {
+  return gateup_impl(kGateUpSwiglu, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T, k, E, H, I, h,
+                     nullptr, ld_h, stream, "moe_mxfp4_gateup_swiglu");
+}
+
+extern "C" moe_status moe_mxfp4_gateup(const int8_t *xq, int64_t ld_xq, const float *xs, int64_t ld_xs,
+                                       const uint8_t *wg, const uint8_t *sg, const uint8_t *wu, const uint8_t *su,
+                                       const int32_t *offsets, const int32_t *sorted, int64_t cap, int T, int k,
+                                       int E, int H, int I, float *g, float *u, int64_t ld_gu, void *stream) {
+  return gateup_impl(kGateUpRaw, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T, k, E, H, I, g, u,
+                     ld_gu, stream, "moe_mxfp4_gateup");
+}
+
+extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *hs, int64_t ld_hs,
+                                     const uint8_t *wd, const uint8_t *sd, const int32_t *offsets,
+                                     const int32_t *sorted, int64_t cap, int T, int k, int E, int H, int I, float *y,
+                                     int64_t ld_y, void *stream) {
+  const char *name = "moe_mxfp4_down";
+  moe_status st = check_common(name, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E,
+                               H, I, y, ld_y, I, T * k);
+  if (st != MOE_OK || T == 0) return st;
+  if (ld_y < H) return fail(MOE_ERR_INVALID_ARG, "%s: ld_y=%lld < H=%d", name, (long long)ld_y, H);
+  MxArgs p{};
+  p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
+  p.w0 = wd; p.s0 = sd;
+  p.offsets = offsets; p.sorted = sorted; p.cap = cap;
+  p.A = T * k; p.k = k; p.E = E; p.K = I; p.N = H;
+  p.out0 = y; p.ld_out = ld_y;
+  p.status = device_status_word();
+  return launch_mx<kDown>(p, static_cast<cudaStream_t>(stream), name);
+}

@@ -1,0 +1,116 @@
+"""One MoE layer forward as the sequence of C-ABI calls.
+
+The layer of the DeepSeek-V4-Flash pages ("DeepSeek-V4-Flash on AMD gfx90a",
+Fig. 1): route top-k -> sort -> Q8(x) -> gate/up + SwiGLU -> Q8(h) -> down ->
+slot-ordered combine.  This module only allocates device buffers (through
+PyTorch) and issues the calls; it computes nothing itself.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import (act_quant_q8, moe_combine, moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk,
+               moe_sort_tokens, moe_sort_tokens_capacity)
+
+
+@dataclasses.dataclass
+class LayerWeights:
+    """Device weights of one layer in the boundary layout (see moe_mxfp4.h)."""
+    wr: torch.Tensor            # [E, H] router, float32 or bfloat16
+    bias: torch.Tensor | None   # [E] float32 logit bias or None
+    wg: torch.Tensor            # [E, I, H/2] uint8
+    sg: torch.Tensor            # [E, I, H/32] uint8
+    wu: torch.Tensor
+    su: torch.Tensor
+    wd: torch.Tensor            # [E, H, I/2] uint8
+    sd: torch.Tensor            # [E, H, I/32] uint8
+    k: int
+
+    @property
+    def E(self):
+        return self.wr.shape[0]
+
+    @property
+    def H(self):
+        return self.wr.shape[1]
+
+    @property
+    def I(self):
+        return self.wg.shape[1]
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.wr, self.wg, self.sg, self.wu, self.su, self.wd, self.sd))
+
+
+class Workspace:
+    """Every intermediate of one forward over T tokens (device tensors).
+
+    ``pad`` adds that many extra columns to every 2-D buffer (rounded to keep
+    16-byte row alignment), so the calls run on padded row strides.
+    """
+
+    def __init__(self, T: int, lw: LayerWeights, device, pad: int = 0, tile_rows: int = 1):
+        H, E, k, I = lw.H, lw.E, lw.k, lw.I
+        A = T * k
+        p16 = (pad + 15) // 16 * 16
+
+        def buf(rows, cols, dtype, align_cols=1):
+            extra = p16 if pad else 0
+            extra = (extra + align_cols - 1) // align_cols * align_cols
+            full = torch.empty(rows, cols + extra, dtype=dtype, device=device)
+            return full[:, :cols]
+
+        self.T, self.A, self.tile_rows = T, A, tile_rows
+        self.logits = buf(T, E, torch.float32)
+        self.ids = torch.empty(T, k, dtype=torch.int32, device=device)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+        cap = moe_sort_tokens_capacity(T, k, E, tile_rows)
+        self.sorted = torch.empty(max(cap, 1), dtype=torch.int32, device=device)
+        self.inv = torch.empty(max(A, 1), dtype=torch.int32, device=device)
+        self.xq = buf(T, H, torch.int8, 16)
+        self.xs = buf(T, H // 32, torch.float32)
+        self.h = buf(A, I, torch.float32)
+        self.hq = buf(A, I, torch.int8, 16)
+        self.hs = buf(A, I // 32, torch.float32)
+        self.y = buf(A, H, torch.float32)
+        self.out = buf(T, H, torch.float32)
+
+
+class MoeLayer:
+    def __init__(self, weights: LayerWeights):
+        self.lw = weights
+
+    def forward(self, x: torch.Tensor, ws: Workspace, stream=None, events: dict | None = None) -> torch.Tensor:
+        """out = MoE(x) for the T rows of x ([T, H] bf16/f32, unit column stride).
+
+        ``events`` optionally maps a stage name ("route", "sort", "quant_x",
+        "gateup", "quant_h", "down", "combine") to a (start, end) pair of
+        torch.cuda.Event recorded around that stage on ``stream``."""
+        lw = self.lw
+        s = torch.cuda.current_stream() if stream is None else stream
+        ev = events or {}
+
+        def stage(name, fn, *args):
+            if name in ev:
+                ev[name][0].record(s)
+            fn(*args, stream=s)
+            if name in ev:
+                ev[name][1].record(s)
+
+        stage("route", moe_route_topk, x, lw.wr, lw.bias, lw.k, ws.logits, ws.ids, ws.w)
+        stage("sort", moe_sort_tokens, ws.ids, lw.E, ws.tile_rows, ws.offsets, ws.sorted, ws.inv)
+        stage("quant_x", act_quant_q8, x, ws.xq, ws.xs)
+        stage("gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, lw.wg, lw.sg, lw.wu, lw.su, ws.offsets, ws.sorted,
+              lw.k, ws.h)
+        stage("quant_h", act_quant_q8, ws.h, ws.hq, ws.hs)
+        stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
+        stage("combine", moe_combine, ws.y, ws.w, ws.out)
+        return ws.out
+
+    # launches per forward, for launch accounting
+    KERNELS_PER_FORWARD = 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine

@@ -59,6 +59,7 @@ def lib():
             L.moe_oracle_block_dot.restype = C.c_int32
             L.moe_oracle_expert_gateup.argtypes = [P, P, P, P, P, P, C.c_int, C.c_int, P, P]
             L.moe_oracle_expert_down.argtypes = [P, P, P, P, C.c_int, C.c_int, P]
+            L.moe_oracle_combine.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P]
             L.moe_oracle_layer.argtypes = ([P, C.c_int, C.c_int, C.c_int, P, C.c_int, P, C.c_int, C.c_int, C.c_int]
                                            + [P] * 6 + [P] * 10)
             L.moe_oracle_layer.restype = C.c_int
@@ -162,6 +163,16 @@ def expert_down(hq, hs, wd, sd):
     sd = np.ascontiguousarray(sd, dtype=np.uint8)
     lib().moe_oracle_expert_down(_p(hq), _p(hs), _p(wd), _p(sd), H, I, _p(y))
     return y
+
+
+def combine(y: np.ndarray, w: np.ndarray) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    T, k = w.shape
+    H = y.shape[1]
+    out = np.empty((T, H), dtype=np.float64)
+    lib().moe_oracle_combine(_p(y), _p(w), T, k, H, _p(out))
+    return out
 
 
 def layer(x: np.ndarray, wr: np.ndarray, bias, k: int, experts: dict):

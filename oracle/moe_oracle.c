@@ -205,10 +205,17 @@ void moe_oracle_quant_q8(const void *x, int x_bf16, int rows, int cols, int64_t 
 
 /* ------------------------------------------------------------------ MX dots */
 
-/* Twice the E2M1 value of a nibble, an exact small integer. */
+/* Twice the E2M1 value of a nibble, an exact small integer; the 16 values
+ * are taken once from moe_oracle_e2m1. */
 static int e2m1_twice(int code)
 {
-    return (int)lround(2.0 * moe_oracle_e2m1(code));
+    static int table[16];
+    static int ready = 0;
+    if (!ready) {
+        for (int c = 0; c < 16; ++c) table[c] = (int)lround(2.0 * moe_oracle_e2m1(c));
+        ready = 1;
+    }
+    return table[code];
 }
 
 /* Exact integer block dot I = sum_{l<32} q_l * 2*e2m1(c_l) over one 32-element
@@ -271,6 +278,19 @@ void moe_oracle_expert_down(const int8_t *hq, const float *hs,
         y[n] = mx_dot(hq, hs, wd + (int64_t)n * (I / 2), sd + (int64_t)n * (I / 32), I);
 }
 
+/* Routing-weighted combine, slot order, fp64 ([GFX] §8.2 "FP32 top-k partial
+ * and fixed reduction"): out[t,n] = sum_{j<k} w[t,j] * y[t*k+j, n]. */
+void moe_oracle_combine(const double *y, const double *w, int T, int k, int H, double *out)
+{
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j)
+                acc += w[(int64_t)t * k + j] * y[((int64_t)t * k + j) * H + n];
+            out[(int64_t)t * H + n] = acc;
+        }
+}
+
 /* ------------------------------------------------------------------ layer */
 
 /* The routed-expert MoE layer for T tokens ([GFX] Fig. 1, [SH] "MXFP4
@@ -318,15 +338,7 @@ int moe_oracle_layer(const void *x, int x_bf16, int T, int H,
         moe_oracle_quant_q8(hf, 0, 1, I, I, hq + a * I, I, hs + a * (I / 32), I / 32);
         moe_oracle_expert_down(hq + a * I, hs + a * (I / 32), wd[e], sd[e], H, I, y + a * H);
     }
-    if (rc == 0) {
-        for (int t = 0; t < T; ++t)
-            for (int n = 0; n < H; ++n) {
-                double acc = 0.0;
-                for (int j = 0; j < k; ++j)
-                    acc += w[(int64_t)t * k + j] * y[((int64_t)t * k + j) * H + n];
-                out[(int64_t)t * H + n] = acc;
-            }
-    }
+    if (rc == 0) moe_oracle_combine(y, w, T, k, H, out);
     free(G);
     free(U);
     free(hf);

@@ -1,0 +1,239 @@
+"""Stage-by-stage parity of the CUDA path against the oracle, through the C ABI.
+
+Integer and index work (router logits that decide the top-k, top-k ids, the
+sort, Q8 codes and scales, exact integer block dots) must match bit for bit;
+fp32 results must be within 1e-3 * RMS of the oracle's fp64 values.  Every
+stage is also run on padded row strides, on ragged shapes (sizes that leave
+lanes of the last block group idle, E not a multiple of 32) and on empty input.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, bits_equal, dev, ensure_built, host, max_err_over_rms
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return ensure_built()
+
+
+def _spec(name):
+    return {"tiny": synth.TINY, "dsv4": synth.DSV4, "zipf": synth.DSV4_ZIPF,
+            "odd": synth.LayerSpec(H=384, E=40, k=3, I=640, x_dtype="bf16", wr_dtype="f32", seed=5)}[name]
+
+
+# ----------------------------------------------------------------- router
+
+@pytest.mark.parametrize("name,T,pad", [("tiny", 1, 0), ("tiny", 7, 24), ("dsv4", 1, 0), ("dsv4", 16, 8),
+                                        ("dsv4", 37, 0), ("zipf", 64, 0), ("odd", 9, 40)])
+def test_route_topk(moe, name, T, pad):
+    spec = _spec(name)
+    x = synth.activations(spec, T, token0=3)
+    wr = synth.router_weights(spec)
+    bias = synth.router_bias(spec)
+    logits_o, ids_o, w_o = oracle.route(x, wr, spec.k, bias)
+    xd = dev(x, pad)
+    logits = torch.empty(T, spec.E, device="cuda")
+    ids = torch.empty(T, spec.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, spec.k, device="cuda")
+    moe.moe_route_topk(xd, dev(wr), None if bias is None else dev(bias), spec.k, logits, ids, w)
+    assert bits_equal(host(logits), logits_o)
+    assert np.array_equal(host(ids), ids_o)
+    assert np.allclose(host(w), w_o, rtol=2e-6, atol=0)
+
+
+def test_route_topk_ties(moe):
+    # identical router rows: equal logits, ties go to the lower expert id
+    spec = synth.LayerSpec(H=256, E=64, k=6, I=128, x_dtype="f32", wr_dtype="f32")
+    wr = synth.router_weights(spec)
+    wr[10] = wr[40]
+    wr[3] = wr[40]
+    x = synth.activations(spec, 5)
+    logits_o, ids_o, w_o = oracle.route(x, wr, spec.k)
+    logits = torch.empty(5, 64, device="cuda")
+    ids = torch.empty(5, 6, dtype=torch.int32, device="cuda")
+    w = torch.empty(5, 6, device="cuda")
+    moe.moe_route_topk(dev(x), dev(wr), None, 6, logits, ids, w)
+    assert np.array_equal(host(ids), ids_o)
+
+
+# ----------------------------------------------------------------- sort
+
+@pytest.mark.parametrize("T,k,E,tile", [(1, 6, 256, 1), (16, 6, 256, 1), (37, 2, 8, 1), (1500, 6, 256, 1),
+                                        (512, 6, 256, 64), (8192, 6, 256, 1), (64, 8, 40, 16), (3, 1, 1, 1)])
+def test_sort(moe, T, k, E, tile):
+    ids = (synth.raw_u64(9, 800 + T, 0, T * k) % np.uint64(E)).astype(np.int32).reshape(T, k)
+    if T == 64:  # skew: half of all assignments on one expert
+        ids[: T // 2, 0] = 7
+    off_o, srt_o, inv_o = oracle.sort(ids, E, tile)
+    cap = moe.moe_sort_tokens_capacity(T, k, E, tile)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    srt = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    moe.moe_sort_tokens(dev(ids), E, tile, offsets, srt, inv)
+    assert np.array_equal(host(offsets), off_o)
+    assert np.array_equal(host(srt)[: off_o[-1]], srt_o)
+    assert np.array_equal(host(inv), inv_o)
+    assert moe.moe_device_status() == 0
+
+
+def test_sort_flags_bad_ids(moe):
+    ids = np.array([[1, 2], [9, 0], [-1, 3]], np.int32)
+    offsets = torch.empty(5, dtype=torch.int32, device="cuda")
+    srt = torch.empty(6, dtype=torch.int32, device="cuda")
+    inv = torch.empty(6, dtype=torch.int32, device="cuda")
+    moe.moe_sort_tokens(dev(ids), 4, 1, offsets, srt, inv)
+    assert moe.moe_device_status() & moe.MOE_DEV_BAD_EXPERT_ID
+    good = np.array([[1, 2], [0, 0], [0, 3]], np.int32)  # the valid ones, in place
+    inv_h = host(inv)
+    assert inv_h[2] == -1 and inv_h[4] == -1
+    assert list(host(offsets)) == [0, 1, 2, 3, 4]
+    assert list(host(srt)[:4]) == [3, 0, 1, 5]
+    del good
+
+
+def test_sort_empty(moe):
+    offsets = torch.full((9,), 5, dtype=torch.int32, device="cuda")
+    srt = torch.empty(1, dtype=torch.int32, device="cuda")
+    inv = torch.empty(1, dtype=torch.int32, device="cuda")
+    moe.moe_sort_tokens(torch.empty(0, 2, dtype=torch.int32, device="cuda"), 8, 1, offsets, srt, inv)
+    assert list(host(offsets)) == [0] * 9
+
+
+# ----------------------------------------------------------------- Q8
+
+@pytest.mark.parametrize("rows,cols,dt,pad", [(1, 4096, "bf16", 0), (3, 256, "f32", 0), (97, 2048, "f32", 32),
+                                              (513, 4096, "bf16", 64), (5, 32, "f32", 0)])
+def test_quant_q8(moe, rows, cols, dt, pad):
+    x = synth.normal(2, 900 + rows, 0, rows * cols).astype(np.float32).reshape(rows, cols)
+    x *= np.repeat(synth.positive_scales(2, 901, rows, cols // 32, 1e-4, 1e4), 32, axis=1)
+    x[0, :32] = 0.0                       # an all-zero block
+    x[-1, -32:] = np.float32(2.5)         # a constant block
+    if dt == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    q_o, s_o = oracle.quant_q8(x)
+    xd = dev(x, pad)
+    qfull = torch.empty(rows, cols + pad, dtype=torch.int8, device="cuda")
+    q = qfull[:, :cols]
+    sfull = torch.empty(rows, cols // 32 + pad, dtype=torch.float32, device="cuda")
+    s = sfull[:, : cols // 32]
+    moe.act_quant_q8(xd, q, s)
+    assert bits_equal(host(q), q_o)
+    assert bits_equal(host(s), s_o)
+
+
+def test_quant_q8_empty(moe):
+    moe.act_quant_q8(torch.empty(0, 64, device="cuda"), torch.empty(0, 64, dtype=torch.int8, device="cuda"),
+                     torch.empty(0, 2, device="cuda"))
+
+
+# ----------------------------------------------------------------- projections
+
+def _route_rows(T, k, E, seed):
+    ids = np.empty((T, k), np.int32)
+    for t in range(T):
+        r = synth.raw_u64(seed, 1000 + t, 0, E)
+        ids[t] = np.argsort(r, kind="stable")[:k].astype(np.int32)
+    return ids
+
+
+def _experts(spec, E):
+    return {e: synth.expert(spec, e) for e in range(E)}
+
+
+def _stack(experts, E, name):
+    return torch.from_numpy(np.stack([getattr(experts[e], name) for e in range(E)])).cuda()
+
+
+@pytest.mark.parametrize("H,I,E,k,T,exact", [(4096, 256, 3, 2, 5, True), (256, 128, 8, 2, 3, True),
+                                             (384, 640, 5, 3, 4, True), (4096, 256, 3, 2, 5, False),
+                                             (512, 384, 6, 6, 17, False)])
+def test_gateup(moe, H, I, E, k, T, exact):
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=21)
+    ex = _experts(spec, E)
+    if exact:
+        # xs = 1 and every E8M0 byte 128 (factor 2^(128-128) = 1): G and U are
+        # the exact integer sums of the block dots, representable in fp32.
+        for e in ex.values():
+            e.sg[:] = 128
+            e.su[:] = 128
+        xs = np.ones((T, H // 32), np.float32)
+    else:
+        xs = synth.positive_scales(21, 1101, T, H // 32)
+    xq = synth.int8_codes(21, 1100, T, H)
+    ids = _route_rows(T, k, E, 21)
+    offsets, srt, _ = oracle.sort(ids, E, 1)
+    Go = np.zeros((T * k, I))
+    Uo = np.zeros((T * k, I))
+    for a in range(T * k):
+        e = ex[ids.ravel()[a]]
+        Go[a], Uo[a] = oracle.expert_gateup(xq[a // k], xs[a // k], e.wg, e.sg, e.wu, e.su)
+    g = torch.full((T * k, I), float("nan"), device="cuda")
+    u = torch.full((T * k, I), float("nan"), device="cuda")
+    W = {n: _stack(ex, E, n) for n in ("wg", "sg", "wu", "su")}
+    moe.moe_mxfp4_gateup(dev(xq, 16), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets), dev(srt), k, g, u)
+    if exact:
+        assert bits_equal(host(g), Go.astype(np.float32))
+        assert bits_equal(host(u), Uo.astype(np.float32))
+    else:
+        assert max_err_over_rms(host(g), Go) <= 1e-5
+        assert max_err_over_rms(host(u), Uo) <= 1e-5
+    # SwiGLU output: h = silu(G) * U
+    h = torch.full((T * k, I + 8), float("nan"), device="cuda")[:, :I]
+    moe.moe_mxfp4_gateup_swiglu(dev(xq), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets), dev(srt), k, h)
+    ho = np.vectorize(oracle.silu)(Go) * Uo
+    assert max_err_over_rms(host(h), ho) <= TOL
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("H,I,E,k,T,exact", [(4096, 2048, 3, 2, 3, True), (256, 128, 8, 2, 3, True),
+                                             (384, 640, 5, 3, 4, False), (4096, 2048, 2, 2, 4, False)])
+def test_down(moe, H, I, E, k, T, exact):
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=22)
+    ex = _experts(spec, E)
+    A = T * k
+    if exact:
+        for e in ex.values():
+            e.sd[:] = 128
+        hs = np.ones((A, I // 32), np.float32)
+    else:
+        hs = synth.positive_scales(22, 1201, A, I // 32)
+    hq = synth.int8_codes(22, 1200, A, I)
+    ids = _route_rows(T, k, E, 22)
+    offsets, srt, _ = oracle.sort(ids, E, 4)   # padded segments: -1 rows are skipped
+    yo = np.zeros((A, H))
+    for a in range(A):
+        e = ex[ids.ravel()[a]]
+        yo[a] = oracle.expert_down(hq[a], hs[a], e.wd, e.sd)
+    y = torch.full((A, H + 4), float("nan"), device="cuda")[:, :H]
+    srt_full = np.concatenate([srt, np.full(E * 3 + A - srt.size, -1, np.int32)])
+    moe.moe_mxfp4_down(dev(hq, 32), dev(hs), _stack(ex, E, "wd"), _stack(ex, E, "sd"), dev(offsets),
+                       dev(srt_full), T, k, y)
+    if exact:
+        assert bits_equal(host(y), yo.astype(np.float32))
+    else:
+        assert max_err_over_rms(host(y), yo) <= 1e-5
+    assert moe.moe_device_status() == 0
+
+
+def test_combine(moe):
+    T, k, H = 9, 6, 4096
+    y = synth.normal(3, 1300, 0, T * k * H).astype(np.float32).reshape(T * k, H)
+    w = synth.uniform01(3, 1301, 0, T * k).astype(np.float32).reshape(T, k)
+    ref = oracle.combine(y.astype(np.float64), w.astype(np.float64))
+    out = torch.empty(T, H + 16, device="cuda")[:, :H]
+    moe.moe_combine(dev(y, 8), dev(w), out)
+    assert max_err_over_rms(host(out), ref) <= 1e-6
+
+
+def test_empty_calls_are_noops(moe):
+    lw_ids = torch.empty(0, 6, dtype=torch.int32, device="cuda")
+    out = torch.full((1, 256), 3.0, device="cuda")
+    moe.moe_combine(torch.empty(0, 256, device="cuda"), torch.empty(0, 6, device="cuda"), out[:0])
+    assert torch.all(out == 3.0)
+    del lw_ids

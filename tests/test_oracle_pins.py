@@ -275,6 +275,18 @@ def test_sort_padding():
     assert np.array_equal(srt[inv], np.arange(6))
 
 
+def test_combine_matches_weighted_sum():
+    y = synth.normal(8, 700, 0, 12 * 64).reshape(12, 64)
+    w = synth.uniform01(8, 701, 0, 4 * 3).reshape(4, 3)
+    out = oracle.combine(y, w)
+    ref = np.einsum("tj,tjn->tn", w, y.reshape(4, 3, 64))
+    assert np.allclose(out, ref, rtol=1e-14, atol=1e-14)
+    # slot j of token t is row t*k + j
+    w1 = np.zeros((4, 3))
+    w1[2, 1] = 1.0
+    assert np.array_equal(oracle.combine(y, w1)[2], y[2 * 3 + 1])
+
+
 # --------------------------------------------------------------- layer
 
 def _textbook_layer(x_f32, wr_f32, bias, k, experts, E):
