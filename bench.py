@@ -276,6 +276,7 @@ def main():
     xs = torch.randn(NX, T, H, generator=gx, device=dev).to(torch.bfloat16)
     ws = moe.Workspace(T, layers[0], dev)
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)  # weights, inputs and workspace are written on the default stream
 
     # ---- capture one graph per (layer, batch), gate/up bracketed by events
     try:
@@ -285,12 +286,14 @@ def main():
     except TypeError:
         in_graph_events = False
     graphs, gu_events = [], []
+    fused = moe.MoeLayer(layers[0]).use_fused(T)
+    stage = "decode" if fused else "gateup"   # the dominant kernel
     with torch.cuda.stream(stream):
         for gi in range(NG):
             lw, x = layers[gi % NL], xs[(gi // NL) % NX]
             layer = moe.MoeLayer(lw)
             layer.forward(x, ws, stream)  # warm / first-call set-up outside capture
-            ev = {"gateup": (mk_ev(), mk_ev())} if in_graph_events else None
+            ev = {stage: (mk_ev(), mk_ev())} if in_graph_events else None
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 layer.forward(x, ws, stream, events=ev)
@@ -306,7 +309,10 @@ def main():
         uniq.append(int(torch.unique(ws.ids).numel()))
     A = T * K_TOP
     step_bytes = [ROUTER_BYTES + u * EXPERT_BYTES + T * H * 2 + T * H * 4 for u in uniq]
-    gu_bytes = [u * 2 * I_EXP * (H // 2 + H // 32) + T * (H + H // 32 * 4) + A * I_EXP * 4 for u in uniq]
+    if fused:  # the one kernel moves the whole layer
+        gu_bytes = step_bytes
+    else:
+        gu_bytes = [u * 2 * I_EXP * (H // 2 + H // 32) + T * (H + H // 32 * 4) + A * I_EXP * 4 for u in uniq]
 
     # ---- warm-up: W steps, plus enough to bring clocks up (~0.3 s)
     def run(n, start=0):
@@ -339,7 +345,7 @@ def main():
     ms = ev0.elapsed_time(ev1)
     last = [(s % NG) for s in range(max(0, K - NG), K)]
     if in_graph_events:
-        gu_ms = [gu_events[g]["gateup"][0].elapsed_time(gu_events[g]["gateup"][1]) for g in last]
+        gu_ms = [gu_events[g][stage][0].elapsed_time(gu_events[g][stage][1]) for g in last]
     else:
         gu_ms = []
     if dist:
@@ -398,7 +404,7 @@ def main():
     if gu_ms:
         gb = sum(gu_bytes[g] for g in last)
         achieved = gb / (sum(gu_ms) * 1e-3) / 1e9
-        roofline = {"kernel": "moe_mxfp4_gateup_swiglu", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+        roofline = {"kernel": "moe_decode_forward" if fused else "moe_mxfp4_gateup_swiglu", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
                     "peak_kind": peak_kind, "launches_timed": len(gu_ms),
                     "avg_launch_us": 1e3 * sum(gu_ms) / len(gu_ms),
@@ -421,12 +427,13 @@ def main():
                        "zipf_bias": zipf, "parallelism": f"replicas{world}",
                        "l2": f"{NL} layer copies x {NX} token batches cycled ({NL * 3.42:.1f} GB of weights > L2)",
                        "graph": "one CUDA graph per (layer copy, batch), replayed back to back",
+                       "path": "fused single-launch decode" if fused else "six stage calls (8 kernels)",
                        "distinct_experts_mean": sum(uniq) / len(uniq)},
             "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * moe.MoeLayer.KERNELS_PER_FORWARD,
+            "gpu_launches": K * moe.MoeLayer(layers[0]).kernels_per_forward(T),
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -204,6 +204,49 @@ MOE_API moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *
 MOE_API moe_status moe_combine(const float *y, int64_t ld_y, const float *w, int T, int k, int H,
                        float *out, int64_t ld_out, void *stream);
 
+/* ---------------------------------------------------------------- fused decode */
+
+/* Bytes of the workspace moe_decode_forward needs (grid-barrier counters). */
+MOE_API size_t moe_decode_workspace_bytes(void);
+
+/* Largest T that moe_decode_forward accepts for this layer shape on the
+ * current device (0: none; needs the CUDA device to be set). */
+MOE_API int moe_decode_max_tokens(int H, int E, int k, int I);
+
+/* The whole layer for a small decode batch in ONE launch: router + top-k +
+ * sort + Q8(x) + gate/up + SwiGLU + Q8(h) + down + combine, with the same
+ * arithmetic as the stage calls above, so every output is bit-identical to
+ * running them in sequence (the Strix Halo record's exact-rows contract:
+ * batching never changes a row's bits).  A cooperative launch of one CTA per
+ * SM; each SM streams its share of every selected expert's weights through a
+ * TMA ring, gate/up slices first, then down slices (prefetched into L2).
+ *  x, w_router, bias, weights: as for the stage calls (x [T][ld_x]).
+ *  out      [T][ld_out] fp32 output (the layer output).
+ *  logits   [T][E], ids [T][k], weights [T][k]: outputs, as moe_route_topk.
+ *  h        [T*k][ld_h] fp32: the SwiGLU activations (output; also the
+ *           exchange buffer between the two projections; 16-byte aligned,
+ *           ld_h a multiple of 4).
+ *  y        [T*k][ld_y] fp32 per-slot down outputs, or NULL.
+ *  workspace  >= moe_decode_workspace_bytes(), 8-byte aligned, zero-filled
+ *           before its first use; each call leaves it ready for the next.
+ *           Calls that share a workspace must not run concurrently.
+ * Requires T <= moe_decode_max_tokens(H, E, k, I) (T*k <= 64, T <= 14, and the
+ * activation rows must fit shared memory; else MOE_ERR_UNSUPPORTED: use the
+ * stage calls), plus the stage calls' shape rules (H, I multiples of 128,
+ * <= 4096).
+ * A wait that does not complete (a device fault elsewhere) sets
+ * MOE_DEV_WAIT_TIMEOUT and the launch returns with outputs incomplete; the
+ * workspace must then be zero-filled again. */
+MOE_API moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t ld_x,
+                                      const void *w_router, moe_dtype w_dtype, const float *bias,
+                                      const uint8_t *wg, const uint8_t *sg, const uint8_t *wu, const uint8_t *su,
+                                      const uint8_t *wd, const uint8_t *sd,
+                                      int T, int H, int E, int k, int I,
+                                      float *out, int64_t ld_out,
+                                      float *logits, int32_t *ids, float *weights,
+                                      float *h, int64_t ld_h, float *y, int64_t ld_y,
+                                      void *workspace, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

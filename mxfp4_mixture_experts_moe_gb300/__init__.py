@@ -27,7 +27,8 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
-           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine"]
+           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_decode_workspace_bytes",
+           "moe_decode_max_tokens", "moe_decode_forward"]
 
 _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 _SIG = {
@@ -42,6 +43,10 @@ _SIG = {
     "moe_mxfp4_gateup": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _P, _L, _P]),
     "moe_mxfp4_down": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _L, _P]),
     "moe_combine": (_I, [_P, _L, _P, _I, _I, _I, _P, _L, _P]),
+    "moe_decode_workspace_bytes": (C.c_size_t, []),
+    "moe_decode_max_tokens": (_I, [_I, _I, _I, _I]),
+    "moe_decode_forward": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L] + [_P] * 3
+                           + [_P, _L, _P, _L, _P, C.c_size_t, _P]),
 }
 library_path = _LIB_PATH
 
@@ -176,6 +181,25 @@ def moe_combine(y, w, out, stream=None):
     T, k = w.shape
     H = out.shape[1]
     _check(_lib.moe_combine(_ptr(y), _ld(y), _ptr(w), T, k, H, _ptr(out), _ld(out), _stream(stream)))
+
+
+def moe_decode_workspace_bytes() -> int:
+    return _lib.moe_decode_workspace_bytes()
+
+
+def moe_decode_max_tokens(H, E, k, I) -> int:
+    return _lib.moe_decode_max_tokens(H, E, k, I)
+
+
+def moe_decode_forward(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out, logits, ids, weights, h, y, workspace,
+                       stream=None):
+    T, H = x.shape[0], w_router.shape[1]
+    E, I = w_router.shape[0], wg.shape[1]
+    _check(_lib.moe_decode_forward(_ptr(x), _dt(x), _ld(x), _ptr(w_router), _dt(w_router), _ptr(bias),
+                                   _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(wd), _ptr(sd), T, H, E, k, I,
+                                   _ptr(out), _ld(out), _ptr(logits), _ptr(ids), _ptr(weights), _ptr(h), _ld(h),
+                                   _ptr(y), _ld(y) if y is not None else 0, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 from .layer import MoeLayer, LayerWeights, Workspace  # noqa: E402

@@ -25,8 +25,8 @@ int sm_count();
 // the integer block dots count twice the E2M1 values).  Exact for every byte
 // (subnormal for u < 2); byte 255 is NaN.
 MOE_DEVFN float e8m0_half(uint32_t u) {
-  uint32_t bits = (u >= 2u) ? ((u - 1u) << 23) : (0x00400000u >> (1u - u));
-  bits = (u == 255u) ? 0x7FC00000u : bits;
+  if (u - 2u < 253u) return __uint_as_float((u - 1u) << 23);  // bytes 2..254: normal fp32
+  const uint32_t bits = (u == 255u) ? 0x7FC00000u : (0x00400000u >> (1u - u));
   return __uint_as_float(bits);
 }
 

@@ -1,0 +1,707 @@
+// Fused single-launch forward of the MoE layer for small decode batches.
+//
+// The same layer as the six stage calls ("DeepSeek-V4-Flash on AMD gfx90a",
+// Fig. 1 and §6.1; "Optimizing DeepSeek V4 Flash Inference on a Strix Halo
+// Pair", "MXFP4 routed-expert kernels": "MoE decode is pure bandwidth"), with
+// the same arithmetic (every step comes from mx_device.cuh), so it gives the
+// same bits as the stage calls, row for row.  What changes is the schedule:
+// one cooperative launch of one CTA per SM instead of eight kernels.
+//
+//   A   router logits (a warp per expert, experts spread over all CTAs) and,
+//       in every CTA, Q8 of the T activation rows into shared memory
+//   --- grid barrier
+//   A'  every CTA: top-k of every token, stable sort of the assignments
+//   B   one TMA ring per CTA streams the CTA's output slice of every active
+//       expert: first the gate/up slices (h -> global), then the down slices
+//       (prefetched into L2 while gate/up runs)
+//   --- grid barrier (consumer warps only; the producer keeps streaming)
+//   C   Q8 of every h row into shared memory, down projection of the CTA's
+//       slice, then the slot-ordered combine of that slice -> out
+//
+// Waits are bounded: a grid barrier or an mbarrier that does not complete in
+// about a second sets MOE_DEV_WAIT_TIMEOUT and the kernel returns.
+#include <algorithm>
+
+#include "mx_device.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 29;
+constexpr int kThreads = kWarps * 32;
+constexpr int kCons = kWarps - 1;  // warps 0..27 consume (<= 64 registers each); warp 28 produces
+constexpr int kMaxA = 64;          // assignments T*k handled by the fused path
+
+struct DecodeArgs {
+  const void *x;
+  int64_t ld_x;
+  int xbf;
+  const void *wr;
+  int wbf;
+  const float *bias;
+  const uint8_t *wg, *sg, *wu, *su, *wd, *sd;
+  int T, H, E, k, I, A;
+  uint32_t kdiv;  // ceil(2^32 / k)
+  float *out;
+  int64_t ld_out;
+  float *logits;
+  int32_t *ids;
+  float *weights;
+  float *h;
+  int64_t ld_h;
+  float *y;  // optional
+  int64_t ld_y;
+  unsigned long long *bar;  // [0] arrival counter, [1] hold (0)
+  unsigned *status;
+  // geometry (host-computed)
+  int nstage;
+  uint32_t stage_bytes;
+  uint32_t gwreg, gsreg;  // gate/up stage: weight / scale region per matrix
+  uint32_t dwreg;         // down stage: weight region
+  uint32_t xrow, hrow;    // staged activation row bytes
+  uint32_t off_bars, off_act, off_y, off_logit, off_misc;
+  int Rd;                 // max down rows per CTA (row stride of the y slice)
+  int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
+  int g16, d16;           // scale bytes copyable in 16-byte pieces
+};
+
+struct Misc {  // views into the small shared-memory region (A = T*k <= 64)
+  int *ids;     // [A] expert of assignment a
+  float *w;     // [A] routing weight of assignment a
+  int *srt;     // [A] assignment at sorted position p
+  int *skey;    // [A] expert at sorted position p
+  int *segb;    // [A+1] start of the j-th expert segment (segb[nact] = A)
+  int *active;  // [A] expert of the j-th segment, increasing id
+  int *scalars; // [0] number of segments, [1] barrier flag
+  float *gu;    // [2][T][Rg][2] gate/up sums of the expert in flight (double buffer)
+};
+
+MOE_DEVFN Misc misc_view(uint8_t *base, int A) {
+  Misc m;
+  int *p = reinterpret_cast<int *>(base);
+  m.ids = p; p += A;
+  m.w = reinterpret_cast<float *>(p); p += A;
+  m.srt = p; p += A;
+  m.skey = p; p += A;
+  m.segb = p; p += A + 1;
+  m.active = p; p += A;
+  m.scalars = p; p += 4;
+  m.gu = reinterpret_cast<float *>(p);
+  return m;
+}
+
+constexpr uint64_t kBarrierTimeoutNs = 250ull * 1000 * 1000;  // 0.25 s
+
+MOE_DEVFN uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Grid-wide barrier for the `nthreads` threads of every CTA that reach it
+// (named barrier `bar_id` inside the CTA).  The workspace holds a 64-bit
+// arrival counter that only grows: each call adds G per barrier, so the
+// counter is a multiple of G between calls; a CTA reads it at kernel start
+// and rounds down (no CTA can pass barrier 1 before every CTA has started),
+// and barrier i completes when the counter reaches base + i*G + hold, where
+// `hold` is workspace word 1 (0 in use; a test sets it to make the wait run
+// out).  Arrival is a fire-and-forget release add; waiting polls with acquire
+// loads for at most kBarrierTimeoutNs.  Returns false on timeout.
+MOE_DEVFN bool grid_barrier(unsigned long long *ctr, unsigned long long target, int bar_id, int nthreads, int *flag,
+                            unsigned *status) {
+  bar_sync_named(bar_id, nthreads);
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ctr), "l"(1ull) : "memory");
+    const uint64_t t0 = globaltimer_ns();
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if (i > (1u << 26) || globaltimer_ns() - t0 > kBarrierTimeoutNs) {
+        ok = 0;
+        break;
+      }
+      if (i >= 8) __nanosleep(32);
+    }
+    if (!ok && status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+    *reinterpret_cast<volatile int *>(flag) = ok;
+  }
+  bar_sync_named(bar_id, nthreads);
+  return *reinterpret_cast<volatile int *>(flag) != 0;
+}
+
+// 8 consecutive bf16 / fp32 values from shared memory, widened exactly.
+MOE_DEVFN void load8_smem(uint32_t addr, bool bf16, float (&v)[8]) {
+  if (bf16) {
+    const uint4 r = lds128(addr);
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+    v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
+  } else {
+    const uint4 a = lds128(addr), b = lds128(addr + 16);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+  }
+}
+
+MOE_DEVFN void load32_smem(uint32_t addr, bool bf16, float (&v)[32]) {
+  const uint32_t step = bf16 ? 16u : 32u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float w8[8];
+    load8_smem(addr + c * step, bf16, w8);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[8 * c + j] = w8[j];
+  }
+}
+
+// router_logits_warp with the router row and the activation rows in shared
+// memory: the same chunk ownership, fma order and butterfly.
+MOE_DEVFN void router_logits_smem(uint32_t wrow, bool wbf, uint32_t x0, uint32_t xrow_bytes, bool xbf, int nt, int H,
+                                  float (&p)[8]) {
+  const int lane = threadIdx.x & 31;
+  const int nch = H / 8;
+  const uint32_t wstep = wbf ? 16u : 32u, xstep = xbf ? 16u : 32u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) p[j] = 0.0f;
+  for (int c = lane; c < nch; c += 32) {
+    float wv[8];
+    load8_smem(wrow + (uint32_t)c * wstep, wbf, wv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < nt) {
+        float xv[8];
+        load8_smem(x0 + (uint32_t)j * xrow_bytes + (uint32_t)c * xstep, xbf, xv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) p[j] = __fmaf_rn(xv[q], wv[q], p[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < nt) {
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], s));
+    }
+  }
+}
+
+// Q8 of one 32-value block into a staged row (split-half layout with the
+// scale and the exact block sum), optionally also to global codes/scales.
+MOE_DEVFN void q8_to_row(const float (&v)[32], uint32_t row, int K, int b) {
+  const int nb = K / 32;
+  uint32_t pk[8];
+  int sum;
+  const float d = q8_block(v, pk, &sum);
+  sts128(row + 16u * b, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+  sts128(row + 16u * (nb + b), make_uint4(pk[4], pk[5], pk[6], pk[7]));
+  sts32(row + (uint32_t)K + 4u * b, __float_as_uint(d));
+  sts32(row + (uint32_t)K + 4u * (nb + b), (uint32_t)sum);
+}
+
+// Q8 of one 32-value block by a lane pair (lanes 2i, 2i+1; the whole warp
+// must call): each lane holds 16 values (half 0: elements 0..15, half 1:
+// 16..31).  amax and the code sum are combined across the pair; every other
+// step is q8_block's, element by element, so the codes, scale and sum are
+// q8_block's.  Half 0 writes the first half-block plane, the scale and the
+// sum; half 1 the second plane.
+MOE_DEVFN void q8_pair_to_row(const float (&v)[16], int half, bool store, uint32_t row, int K, int b) {
+  const int nb = K / 32;
+  float amax = 0.0f;
+#pragma unroll
+  for (int l = 0; l < 16; ++l) amax = fmaxf(amax, fabsf(v[l]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float inv = d > 0.0f ? __frcp_rn(d) : 0.0f;
+  uint32_t pk[4];
+  int sum = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int qi = __float2int_rn(__fmul_rn(v[4 * c + j], inv));
+      qi = max(-127, min(127, qi));
+      sum += qi;
+      word |= (uint32_t)(qi & 0xFF) << (8 * j);
+    }
+    pk[c] = word;
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  if (store) {
+    sts128(row + 16u * (half ? nb + b : b), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+    if (half == 0) {
+      sts32(row + (uint32_t)K + 4u * b, __float_as_uint(d));
+      sts32(row + (uint32_t)K + 4u * (nb + b), (uint32_t)sum);
+    }
+  }
+}
+
+// Stable sort of the A assignments by expert (ties by assignment index), the
+// order of the stand-alone sorter: assignment a lands at position
+// #{b : (id_b, b) < (id_a, a)}.  One thread per assignment, then one warp
+// cuts the sorted keys into expert segments (increasing expert id).
+// An expert id outside [0, E) (top-k of NaN scores) sorts last as E, is left
+// out of every segment and raises MOE_DEV_BAD_EXPERT_ID: no weight address is
+// ever formed from it.
+MOE_DEVFN void rank_sort(const Misc &m, int A, int E, unsigned *status) {
+  const int tid = threadIdx.x;
+  if (tid < A) {
+    int e = m.ids[tid];
+    if (e < 0 || e >= E) {
+      e = E;
+      if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    }
+    int rank = 0;
+    for (int b = 0; b < A; ++b) {
+      int eb = m.ids[b];
+      if (eb < 0 || eb >= E) eb = E;
+      rank += (eb < e) || (eb == e && b < tid);
+    }
+    m.srt[rank] = tid;
+    m.skey[rank] = e;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const unsigned lt = (1u << lane) - 1u;
+    int cnt = 0;
+    for (int p0 = 0; p0 < A; p0 += 32) {
+      const int q = p0 + lane;
+      const bool st = q < A && m.skey[q] < E && (q == 0 || m.skey[q] != m.skey[q - 1]);
+      const unsigned bal = __ballot_sync(0xffffffffu, st);
+      if (st) {
+        const int j = cnt + __popc(bal & lt);
+        m.segb[j] = q;
+        m.active[j] = m.skey[q];
+      }
+      cnt += __popc(bal);
+    }
+    // the last valid segment ends where the invalid ids (if any) begin
+    int nvalid = 0;
+    for (int q = lane; q < A; q += 32) nvalid += m.skey[q] < E;
+    nvalid = __reduce_add_sync(0xffffffffu, (unsigned)nvalid);
+    if (lane == 0) {
+      m.segb[cnt] = nvalid;
+      m.scalars[0] = cnt;
+    }
+  }
+  __syncthreads();
+}
+
+template <int SG, int SD>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int H = p.H, I = p.I, E = p.E, k = p.k, T = p.T, A = p.A;
+  const int nbH = H / 32, nbI = I / 32;
+  const int nstage = p.nstage;
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bars);
+  uint64_t *empty = full + nstage;
+  const uint32_t act = smem_addr(smem + p.off_act);
+  float *yslice = reinterpret_cast<float *>(smem + p.off_y);
+  float *logit_s = reinterpret_cast<float *>(smem + p.off_logit);
+  const Misc m = misc_view(smem + p.off_misc, A);
+
+  const int nrw = (E + G - 1) / G;  // router warps in this kernel (host ensures <= 8)
+  const uint32_t wsz = p.wbf ? 2u : 4u, xsz = p.xbf ? 2u : 4u;
+  const uint32_t front = smem_addr(smem);  // router rows, then x rows (the ring is not in use yet)
+  const uint32_t xs_smem = front + (uint32_t)nrw * H * wsz;
+  uint64_t *fbar = full + 2 * nstage;
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
+      mbar_init(smem_addr(&empty[s]), kCons);
+    }
+    mbar_init(smem_addr(fbar), 1);
+    fence_mbar_init();
+    // stage this CTA's router rows and the T activation rows with bulk copies
+    int nrows = 0;
+    for (int w = 0; w < nrw; ++w) nrows += (cta + G * w) < E;
+    mbar_arrive_expect_tx(smem_addr(fbar), (uint32_t)nrows * H * wsz + (uint32_t)T * H * xsz);
+    const uint64_t pol = policy_evict_first();
+    for (int w = 0; w < nrw; ++w) {
+      const int e = cta + G * w;
+      if (e < E)
+        bulk_g2s(front + (uint32_t)w * H * wsz, static_cast<const uint8_t *>(p.wr) + (int64_t)e * H * wsz, H * wsz,
+                 smem_addr(fbar), pol);
+    }
+    for (int t = 0; t < T; ++t)
+      bulk_g2s(xs_smem + (uint32_t)t * H * xsz, static_cast<const uint8_t *>(p.x) + (int64_t)t * p.ld_x * xsz, H * xsz,
+               smem_addr(fbar), pol);
+  }
+  __shared__ unsigned long long bar_base;
+  if (tid == 32) {
+    unsigned long long v, hold;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(hold) : "l"(p.bar + 1) : "memory");
+    bar_base = v / (unsigned long long)G * (unsigned long long)G + hold;
+  }
+  __syncthreads();
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(fbar), 0, p.status))) return;
+  const unsigned long long base = bar_base;
+
+  // ---------------------------------------------------------------- A
+  if (warp < nrw) {
+    const int e = cta + G * warp;
+    if (e < E) {
+      for (int t0 = 0; t0 < T; t0 += 8) {
+        const int nt = min(8, T - t0);
+        float pl[8];
+        router_logits_smem(front + (uint32_t)warp * H * wsz, p.wbf != 0, xs_smem + (uint32_t)t0 * H * xsz, H * xsz,
+                           p.xbf != 0, nt, H, pl);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (lane == 0 && j < nt) p.logits[(int64_t)(t0 + j) * E + e] = pl[j];
+      }
+    }
+  } else {
+    const int q0 = tid - nrw * 32, qn = kThreads - nrw * 32;
+    for (int idx = q0; idx < T * nbH; idx += qn) {
+      const int t = idx / nbH, b = idx - t * nbH;
+      float v[32];
+      load32_smem(xs_smem + (uint32_t)t * H * xsz + 32u * b * xsz, p.xbf != 0, v);
+      q8_to_row(v, act + (uint32_t)t * p.xrow, H, b);
+    }
+  }
+  if (!grid_barrier(p.bar, base + (unsigned long long)G, 0, kThreads, &m.scalars[1], p.status)) return;
+
+  // ---------------------------------------------------------------- A'
+  for (int i = tid; i < T * E; i += kThreads) logit_s[i] = ldcg_f32(p.logits + i);
+  __syncthreads();
+  if (warp < T) {
+    int id[8];
+    float wv[8];
+    topk_warp(logit_s + warp * E, p.bias, E, k, id, wv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k && lane == j) {
+        m.ids[warp * k + j] = id[j];
+        m.w[warp * k + j] = wv[j];
+        if (cta == 0) {
+          p.ids[(int64_t)warp * k + j] = id[j];
+          p.weights[(int64_t)warp * k + j] = wv[j];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
+  const int nact = m.scalars[0];
+  const int n0g = (int)((int64_t)cta * I / G), Rg = (int)((int64_t)(cta + 1) * I / G) - n0g;
+  const int n0d = (int)((int64_t)cta * H / G), Rd = (int)((int64_t)(cta + 1) * H / G) - n0d;
+
+  if (warp == kCons) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    const uint32_t gw = (uint32_t)Rg * (H / 2), gs = (uint32_t)Rg * nbH;
+    const uint32_t dw = (uint32_t)Rd * (I / 2), ds = (uint32_t)Rd * nbI;
+    int issued = 0;
+    for (int it = 0; it < 2 * nact; ++it) {
+      const int st = it % nstage;
+      if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
+      const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
+      const uint32_t fb = smem_addr(&full[st]);
+      if (it < nact) {
+        const int64_t row0 = (int64_t)m.active[it] * I + n0g;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, 2 * gw);
+          if (gw > 0) {  // a CTA may own no gate/up rows when I < #SMs
+            bulk_g2s(sbase, p.wg + row0 * (H / 2), gw, fb, pol);
+            bulk_g2s(sbase + p.gwreg, p.wu + row0 * (H / 2), gw, fb, pol);
+          }
+        }
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+          const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
+          const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
+          if (p.g16) {
+            for (uint32_t c = lane; c < gs / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+          } else {
+            for (uint32_t c = lane; c < gs / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+          }
+        }
+      } else {
+        const int64_t row0 = (int64_t)m.active[it - nact] * H + n0d;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, dw);
+          if (dw > 0) bulk_g2s(sbase, p.wd + row0 * (I / 2), dw, fb, pol);
+        }
+        const uint8_t *src = p.sd + row0 * nbI;
+        const uint32_t dst = sbase + p.dwreg;
+        if (p.d16) {
+          for (uint32_t c = lane; c < ds / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+        } else {
+          for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+        }
+      }
+      cp_async_mbar_arrive_noinc(fb);
+      issued = it + 1;
+      // once every gate/up slice is requested, pull this CTA's down slices
+      // into L2 so that the down half of the ring reads from L2
+      if (it == nact - 1 && dw > 0) {
+        for (int j = lane; j < nact; j += 32) {
+          const int64_t row0 = (int64_t)m.active[j] * H + n0d;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + row0 * (I / 2)), "r"(dw) : "memory");
+          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + row0 * nbI), "r"(ds) : "memory");
+        }
+      }
+    }
+    for (int it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
+      mbar_wait(smem_addr(&full[it % nstage]), (it / nstage) & 1, p.status);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // A warp whose wait gave up stops computing but keeps arriving on the ring
+  // and on the named barriers, so no other warp is left waiting on it.
+  bool dead = false;
+  for (int it = 0; it < 2 * nact; ++it) {
+    if (it == nact) {
+      // every CTA's h slice is written: quantise all A rows of h here
+      if (!grid_barrier(p.bar, base + 2ull * G, 2, kCons * 32, &m.scalars[1], p.status)) return;
+      for (int base = warp * 32; base < 2 * A * nbI; base += kCons * 32) {
+        const int idx = base + lane;  // 2 * block + half
+        const bool valid = idx < 2 * A * nbI;
+        const int blk = valid ? idx >> 1 : 0, half = idx & 1;
+        const int a = blk / nbI, b = blk - a * nbI;
+        float v[16];
+        const float *src = p.h + (int64_t)a * p.ld_h + 32 * b + 16 * half;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
+          v[4 * c] = __uint_as_float(r.x);
+          v[4 * c + 1] = __uint_as_float(r.y);
+          v[4 * c + 2] = __uint_as_float(r.z);
+          v[4 * c + 3] = __uint_as_float(r.w);
+        }
+        q8_pair_to_row(v, half, valid, act + (uint32_t)a * p.hrow, I, b);
+      }
+      bar_sync_named(1, kCons * 32);
+    }
+    const int st = it % nstage;
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
+    const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
+    if (dead) {
+      // skip the work
+    } else if (it < nact) {
+      // units (output row r, matrix mm): gate and up of a row are summed by
+      // two warps and meet in shared memory for SwiGLU
+      const int sb = m.segb[it], se = m.segb[it + 1];
+      float *gu = m.gu + (it & 1) * (T * p.Rg * 2);
+      for (int u = warp; u < 2 * Rg; u += kCons) {
+        const int r = u >> 1, mm = u & 1;
+        uint4 wq[1][SG];
+        float ws[1][SG];
+        load_weights_packed<1, SG>(sbase + mm * p.gwreg, 0, sbase + 2 * p.gwreg + mm * p.gsreg, 0, r, H, wq, ws);
+#pragma unroll 1
+        for (int q = sb; q < se; ++q) {
+          const int t = (int)__umulhi((unsigned)m.srt[q], p.kdiv);
+          float acc[1];
+          row_dot_smem_pn<1, SG>(act + (uint32_t)t * p.xrow, H, wq, ws, acc);
+          const float v = reduce_one(acc[0]);
+          if (lane == 0) gu[((q - sb) * p.Rg + r) * 2 + mm] = v;
+        }
+      }
+      bar_sync_named(1, kCons * 32);
+      for (int idx = tid; idx < (se - sb) * Rg; idx += kCons * 32) {
+        const int ql = idx / Rg, r = idx - ql * Rg;
+        const float g = gu[(ql * p.Rg + r) * 2], u = gu[(ql * p.Rg + r) * 2 + 1];
+        p.h[(int64_t)m.srt[sb + ql] * p.ld_h + n0g + r] = __fmul_rn(silu(g), u);
+      }
+    } else {
+      const int j = it - nact;
+      const int sb = m.segb[j], se = m.segb[j + 1];
+      for (int r = warp; r < Rd; r += kCons) {
+        uint4 wq[1][SD];
+        float ws[1][SD];
+        load_weights_packed<1, SD>(sbase, p.dwreg, sbase + p.dwreg, 0, r, I, wq, ws);
+#pragma unroll 1
+        for (int q = sb; q < se; ++q) {
+          const int a = m.srt[q];
+          float acc[1];
+          row_dot_smem_pn<1, SD>(act + (uint32_t)a * p.hrow, I, wq, ws, acc);
+          const float v = reduce_one(acc[0]);
+          if (lane == 0) {
+            yslice[a * p.Rd + r] = v;
+            if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+  }
+  bar_sync_named(1, kCons * 32);
+  // combine of this CTA's output slice, slot order
+  for (int idx = tid; idx < T * Rd; idx += kCons * 32) {
+    const int t = idx / Rd, r = idx - t * Rd;
+    const float *wt = m.w + t * k;
+    float acc = __fmul_rn(wt[0], yslice[(t * k) * p.Rd + r]);
+    for (int j = 1; j < k; ++j) acc = __fmaf_rn(wt[j], yslice[(t * k + j) * p.Rd + r], acc);
+    p.out[(int64_t)t * p.ld_out + n0d + r] = acc;
+  }
+}
+
+using DecodeKernel = void (*)(DecodeArgs);
+
+DecodeKernel pick(int sg, int sd) {
+  if (sg == 1 && sd == 1) return decode_kernel<1, 1>;
+  if (sg == 2 && sd == 1) return decode_kernel<2, 1>;
+  if (sg == 2 && sd == 2) return decode_kernel<2, 2>;
+  if (sg == 4 && sd == 2) return decode_kernel<4, 2>;
+  if (sg == 4 && sd == 4) return decode_kernel<4, 4>;
+  if (sg == 1 && sd == 2) return decode_kernel<1, 2>;
+  if (sg == 2 && sd == 4) return decode_kernel<2, 4>;
+  if (sg == 4 && sd == 1) return decode_kernel<4, 1>;
+  if (sg == 1 && sd == 4) return decode_kernel<1, 4>;
+  return nullptr;
+}
+
+uint32_t align16(uint64_t v) { return (uint32_t)((v + 15) & ~uint64_t(15)); }
+
+// Shared-memory plan of the fused kernel for p.T/H/E/k/I on a device with
+// `optin` bytes per CTA and G SMs.  Returns false when it does not fit.
+bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
+  const int H = p.H, I = p.I, E = p.E, T = p.T, A = p.A;
+  const int nbH = H / 32, nbI = I / 32;
+  const int Rg = (I + G - 1) / G, Rd = (H + G - 1) / G;
+  p.Rd = Rd;
+  p.Rg = Rg;
+  p.gwreg = (uint32_t)Rg * (H / 2);
+  p.gsreg = align16((uint64_t)Rg * nbH);
+  p.dwreg = (uint32_t)Rd * (I / 2);
+  const uint32_t gstage = 2 * (p.gwreg + p.gsreg), dstage = p.dwreg + align16((uint64_t)Rd * nbI);
+  p.stage_bytes = ((gstage > dstage ? gstage : dstage) + 127u) & ~127u;
+  p.xrow = (uint32_t)H + 8u * nbH;
+  p.hrow = (uint32_t)I + 8u * nbI;
+  const uint64_t act_bytes = align16(std::max<uint64_t>((uint64_t)T * p.xrow, (uint64_t)A * p.hrow));
+  const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
+  const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
+  const uint64_t misc_bytes = align16(4ull * (7 * A + 5) + 4ull * 2 * T * Rg * 2);
+  const uint64_t tail = 16ull * 8 + act_bytes + y_bytes + logit_bytes + misc_bytes;
+  const uint64_t budget = (uint64_t)optin - 1024;
+  if (tail >= budget) return false;
+  int ns = (int)((budget - tail) / p.stage_bytes);
+  if (ns > 4) ns = 4;
+  if (ns < 2) return false;
+  p.nstage = ns;
+  // the ring area first holds the CTA's router rows and the activation rows
+  const uint64_t front = (uint64_t)((E + G - 1) / G) * H * (p.wbf ? 2 : 4) + (uint64_t)T * H * (p.xbf ? 2 : 4);
+  const uint64_t ring = std::max<uint64_t>((uint64_t)ns * p.stage_bytes, align16(front));
+  if (ring + tail > budget) return false;
+  p.off_bars = (uint32_t)ring;
+  p.off_act = p.off_bars + 16 * 8;
+  p.off_y = p.off_act + (uint32_t)act_bytes;
+  p.off_logit = p.off_y + (uint32_t)y_bytes;
+  p.off_misc = p.off_logit + (uint32_t)logit_bytes;
+  *smem_out = p.off_misc + misc_bytes;
+  return true;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_decode_workspace_bytes(void) { return 64; }  // [0] counter, [1] hold, spare
+
+extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) {
+  if (H <= 0 || E <= 0 || k <= 0 || k > 8 || I <= 0 || H % 128 || I % 128 || H > 4096 || I > 4096 || E > 1024) return 0;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  const int G = sm_count();
+  if ((E + G - 1) / G > 8) return 0;
+  int best = 0;
+  for (int T = 1; T <= kCons && T * k <= kMaxA; ++T) {
+    DecodeArgs p{};
+    p.T = T; p.H = H; p.E = E; p.k = k; p.I = I; p.A = T * k;
+    p.wbf = 0; p.xbf = 0;  // fp32 router and activations: the larger staging
+    size_t smem = 0;
+    if (plan_smem(p, G, optin, &smem)) best = T;
+    else break;
+  }
+  return best;
+}
+
+extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
+                                         moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg,
+                                         const uint8_t *wu, const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
+                                         int T, int H, int E, int k, int I, float *out, int64_t ld_out,
+                                         float *logits, int32_t *ids, float *weights, float *h, int64_t ld_h,
+                                         float *y, int64_t ld_y, void *workspace, size_t ws_bytes, void *stream) {
+  const char *name = "moe_decode_forward";
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: T=%d H=%d E=%d k=%d I=%d", name, T, H, E, k, I);
+  if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad x dtype", name);
+  if (w_dtype != MOE_F32 && w_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad router dtype", name);
+  if (H % 128 || I % 128) return fail(MOE_ERR_INVALID_ARG, "%s: H=%d and I=%d must be multiples of 128", name, H, I);
+  if (H > 4096 || I > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: H, I <= 4096", name);
+  if (E > 1024) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d > 1024", name, E);
+  if (k > 8 || k > E) return fail(MOE_ERR_INVALID_ARG, "%s: k=%d must be <= min(E, 8)", name, k);
+  if (T == 0) return MOE_OK;
+  const int A = T * k;
+  if (A > kMaxA || T > kCons) return fail(MOE_ERR_UNSUPPORTED, "%s: T*k=%d beyond the fused decode path (<= %d)", name, A, kMaxA);
+  if (!x || !w_router || !wg || !sg || !wu || !su || !wd || !sd || !out || !logits || !ids || !weights || !h || !workspace)
+    return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (ws_bytes < moe_decode_workspace_bytes() || (uintptr_t)workspace % 8) return fail(MOE_ERR_INVALID_ARG, "%s: workspace too small", name);
+  const int xes = x_dtype == MOE_BF16 ? 2 : 4;
+  if (ld_x < H || (ld_x * xes) % 16 || (uintptr_t)x % 16 || (uintptr_t)w_router % 16) return fail(MOE_ERR_INVALID_ARG, "%s: x / router must be 16-byte aligned with 16-byte row strides", name);
+  if ((uintptr_t)wg % 16 || (uintptr_t)wu % 16 || (uintptr_t)wd % 16) return fail(MOE_ERR_INVALID_ARG, "%s: weights must be 16-byte aligned", name);
+  if ((uintptr_t)sg % 4 || (uintptr_t)su % 4 || (uintptr_t)sd % 4) return fail(MOE_ERR_INVALID_ARG, "%s: scale bytes must be 4-byte aligned", name);
+  if (ld_out < H || ld_h < I || (ld_h % 4) || (uintptr_t)h % 16 || (y && ld_y < H)) return fail(MOE_ERR_INVALID_ARG, "%s: bad output strides", name);
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, name);
+  int optin = 0, coop = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (!coop) return fail(MOE_ERR_UNSUPPORTED, "%s: device has no cooperative launch", name);
+  const int G = sm_count();
+  if ((E + G - 1) / G > 8) return fail(MOE_ERR_UNSUPPORTED, "%s: too many experts per SM", name);
+  const int nbH = H / 32, nbI = I / 32;
+  const int SG = (nbH + 31) / 32, SD = (nbI + 31) / 32;
+  const int SGp = SG == 3 ? 4 : SG, SDp = SD == 3 ? 4 : SD;
+  DecodeKernel kern = pick(SGp, SDp);
+  if (!kern) return fail(MOE_ERR_UNSUPPORTED, "%s: shape", name);
+
+  DecodeArgs p{};
+  p.x = x; p.ld_x = ld_x; p.xbf = x_dtype == MOE_BF16;
+  p.wr = w_router; p.wbf = w_dtype == MOE_BF16; p.bias = bias;
+  p.wg = wg; p.sg = sg; p.wu = wu; p.su = su; p.wd = wd; p.sd = sd;
+  p.T = T; p.H = H; p.E = E; p.k = k; p.I = I; p.A = A;
+  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
+  p.out = out; p.ld_out = ld_out; p.logits = logits; p.ids = ids; p.weights = weights;
+  p.h = h; p.ld_h = ld_h; p.y = y; p.ld_y = ld_y;
+  p.bar = static_cast<unsigned long long *>(workspace);
+  p.status = device_status_word();
+
+  size_t smem = 0;
+  if (!plan_smem(p, G, optin, &smem)) return fail(MOE_ERR_UNSUPPORTED, "%s: T=%d does not fit the fused path's shared memory", name, T);
+
+  p.g16 = nbH % 16 == 0 && (uintptr_t)sg % 16 == 0 && (uintptr_t)su % 16 == 0;
+  p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0;
+
+  static bool configured[16][64] = {};
+  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2);
+  if (dev < 64 && !configured[ki][dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+    if (err != cudaSuccess) return cuda_fail(err, name);
+    configured[ki][dev] = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, p);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
+}

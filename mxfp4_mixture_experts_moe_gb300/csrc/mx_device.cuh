@@ -1,0 +1,435 @@
+// Device arithmetic shared by every kernel of the layer.  Each step of the
+// layer has exactly one implementation here, so the stand-alone stage kernels
+// and the fused decode kernel compute the same bits for every row.
+#pragma once
+
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ misc
+
+MOE_DEVFN void bar_sync_named(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+MOE_DEVFN float lds_f32(uint32_t addr) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr));
+  return r;
+}
+MOE_DEVFN int lds_s32(uint32_t addr) {
+  int r;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+MOE_DEVFN void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+MOE_DEVFN void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+MOE_DEVFN float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+MOE_DEVFN float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 8 consecutive inputs (bf16 or fp32) from global memory, widened exactly.
+MOE_DEVFN void load8(const void *base, bool bf16, int64_t elem, float (&v)[8]) {
+  if (bf16) {
+    const uint4 r = ldg_nc(static_cast<const uint16_t *>(base) + elem);
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+    v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
+  } else {
+    const float *p = static_cast<const float *>(base) + elem;
+    const uint4 a = ldg_nc(p), b = ldg_nc(p + 4);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+  }
+}
+
+// ------------------------------------------------------------------ router
+
+// Router logit of one expert for up to 8 tokens, one warp.  Lane l owns the
+// chunks l, l+32, ... of 8 consecutive inputs and accumulates them in
+// increasing order with one fma per element; the 32 partial sums are added by
+// an xor butterfly, whose lane-0 value is ((p0+p16)+(p8+p24))+... .  The
+// router row is read 8 chunks per lane at a time (all loads in flight
+// together); the order of the fmas is unchanged by that batching.
+template <int NB = 8>
+MOE_DEVFN void router_logits_warp(const void *x, bool xbf, int64_t ld_x, const void *wr, bool wbf, int e, int t0,
+                                  int nt, int H, float (&p)[8]) {
+  const int lane = threadIdx.x & 31;
+  const int nch = H / 8;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) p[j] = 0.0f;
+  for (int c0 = lane; c0 < nch; c0 += 32 * NB) {
+    float wv[NB][8];
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+      if (c0 + 32 * i < nch) load8(wr, wbf, (int64_t)e * H + 8 * (c0 + 32 * i), wv[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < nt) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const int c = c0 + 32 * i;
+          if (c < nch) {
+            float xv[8];
+            load8(x, xbf, (int64_t)(t0 + j) * ld_x + 8 * c, xv);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) p[j] = __fmaf_rn(xv[q], wv[i][q], p[j]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], s));
+  }
+}
+
+MOE_DEVFN bool topk_better(float s, int i, float bs, int bi) { return s > bs || (s == bs && i < bi); }
+
+// Top-k of one token, one warp: k rounds of an xor-butterfly argmax over
+// (score desc, id asc); score = logit (+ bias), re-read each round.  Weights:
+// sigmoid of the selected scores over their sum.  Every lane returns the same
+// ids/weights.
+MOE_DEVFN float topk_score(const float *logits_row, const float *bias, int e) {
+  const float v = logits_row[e];
+  return bias ? __fadd_rn(v, bias[e]) : v;
+}
+
+// Order-preserving key of a float score (larger score -> larger key); -0 is
+// first turned into +0 so that the keys tie exactly where the scores compare
+// equal.
+MOE_DEVFN uint32_t score_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;  // bit s: expert lane + 32 s already selected
+  float sel[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ids[j] = 0;
+    sel[j] = 0.0f;
+    if (j < k) {
+      // this lane's best unselected expert (score desc, id asc) ...
+      float bs = -CUDART_INF_F;
+      int bi = 0x7fffffff;
+      for (int s = 0, e = lane; e < E; ++s, e += 32) {
+        if ((taken >> s) & 1u) continue;
+        const float v = topk_score(logits_row, bias, e);
+        if (topk_better(v, e, bs, bi)) {
+          bs = v;
+          bi = e;
+        }
+      }
+      // ... then the warp's: the largest score, and among its holders the
+      // lowest id (the same order as topk_better)
+      const uint32_t key = bi == 0x7fffffff ? 0u : score_key(bs);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const int win = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
+      const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+      if ((win & 31) == lane) taken |= 1u << (win >> 5);
+      sel[j] = ws;
+      ids[j] = win;
+    }
+  }
+  float total = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      sel[j] = __frcp_rn(__fadd_rn(1.0f, expf(-sel[j])));
+      total = __fadd_rn(total, sel[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = j < k ? __fdiv_rn(sel[j], total) : 0.0f;
+}
+
+// ------------------------------------------------------------------ Q8
+
+// Q8 of one block of 32 values: scale = amax/127 (IEEE), q = rne(v * (1/scale))
+// clamped to +-127.  Returns the scale; codes packed 4 per word, element 0 in
+// the low byte; *sum = the exact sum of the 32 codes.
+MOE_DEVFN float q8_block(const float (&v)[32], uint32_t (&packed)[8], int *sum) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) amax = fmaxf(amax, fabsf(v[l]));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float inv = d > 0.0f ? __frcp_rn(d) : 0.0f;
+  int s = 0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int qi = __float2int_rn(__fmul_rn(v[4 * c + j], inv));
+      qi = max(-127, min(127, qi));
+      s += qi;
+      word |= (uint32_t)(qi & 0xFF) << (8 * j);
+    }
+    packed[c] = word;
+  }
+  if (sum) *sum = s;
+  return d;
+}
+
+// ------------------------------------------------------------------ MXFP4 dots
+
+// silu(g) = g / (1 + exp(-g)) with the fast exp and divide (for g < -87 the
+// divide returns 0, the limit of silu).
+MOE_DEVFN float silu(float g) { return __fdividef(g, __fadd_rn(1.0f, __expf(-g))); }
+
+MOE_DEVFN int block_sum8(const uint4 &lo, const uint4 &hi) {
+  int s = 0;
+  s = __dp4a((int)lo.x, 0x01010101, s);
+  s = __dp4a((int)lo.y, 0x01010101, s);
+  s = __dp4a((int)lo.z, 0x01010101, s);
+  s = __dp4a((int)lo.w, 0x01010101, s);
+  s = __dp4a((int)hi.x, 0x01010101, s);
+  s = __dp4a((int)hi.y, 0x01010101, s);
+  s = __dp4a((int)hi.z, 0x01010101, s);
+  s = __dp4a((int)hi.w, 0x01010101, s);
+  return s;
+}
+
+// The blocks b = lane + 32 s of one output row of NM matrices, taken from a
+// shared-memory stage (matrix m's rows start at wbase + m*wstride, its E8M0
+// bytes at sbase + m*sstride), converted once: wq = 12 + 2*E2M1 value per
+// byte, ws = 2^(u-128).
+template <int NM, int S>
+MOE_DEVFN void load_weights(uint32_t wbase, uint32_t wstride, uint32_t sbase, uint32_t sstride, int r, int K,
+                            uint32_t (&wq)[NM][S][8], float (&ws)[NM][S]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      const int b = lane + 32 * s;
+      if (b < nb) {
+        const uint4 raw = lds128(wbase + m * wstride + (uint32_t)r * (K / 2) + 16u * b);
+        e2m1x8_to_off12(raw.x, wq[m][s][0], wq[m][s][1]);
+        e2m1x8_to_off12(raw.y, wq[m][s][2], wq[m][s][3]);
+        e2m1x8_to_off12(raw.z, wq[m][s][4], wq[m][s][5]);
+        e2m1x8_to_off12(raw.w, wq[m][s][6], wq[m][s][7]);
+        ws[m][s] = e8m0_half(lds_u8(sbase + m * sstride + (uint32_t)r * nb + b));
+      }
+    }
+  }
+}
+
+// The same blocks kept packed (4 words per block), for callers that convert
+// per row (fewer live registers; the integer dots are the same).
+template <int NM, int S>
+MOE_DEVFN void load_weights_packed(uint32_t wbase, uint32_t wstride, uint32_t sbase, uint32_t sstride, int r, int K,
+                                   uint4 (&wr)[NM][S], float (&ws)[NM][S]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      const int b = lane + 32 * s;
+      if (b < nb) {
+        wr[m][s] = lds128(wbase + m * wstride + (uint32_t)r * (K / 2) + 16u * b);
+        ws[m][s] = e8m0_half(lds_u8(sbase + m * sstride + (uint32_t)r * nb + b));
+      }
+    }
+  }
+}
+
+// Block term of one activation block against the converted weights:
+// acc[m] = fma(float(I_b), sx * ws, acc[m]), I_b = dot(x, 12 + 2v) - 12*sum(x).
+template <int NM, int S>
+MOE_DEVFN void block_terms(int s, const uint4 &lo, const uint4 &hi, float sx, int xsum,
+                           const uint32_t (&wq)[NM][S][8], const float (&ws)[NM][S], float (&acc)[NM]) {
+  const uint32_t xw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    int d = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d = __dp4a((int)xw[j], (int)wq[m][s][j], d);
+    const int I = d - 12 * xsum;
+    acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, ws[m][s]), acc[m]);
+  }
+}
+
+// An activation row staged in shared memory: the K codes as two planes of
+// 16-byte half blocks (first halves of all blocks, then second halves), then
+// nb fp32 scales, then nb int32 block sums.  Row size K + 8*nb bytes.
+template <int NM, int S>
+MOE_DEVFN void row_dot_smem(uint32_t row, int K, const uint32_t (&wq)[NM][S][8], const float (&ws)[NM][S],
+                            float (&acc)[NM]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int b = lane + 32 * s;
+    if (b < nb) {
+      const uint4 lo = lds128(row + 16u * b), hi = lds128(row + 16u * (nb + b));
+      const float sx = lds_f32(row + (uint32_t)K + 4u * b);
+      const int xsum = lds_s32(row + (uint32_t)K + 4u * (nb + b));
+      block_terms<NM, S>(s, lo, hi, sx, xsum, wq, ws, acc);
+    }
+  }
+}
+
+// row_dot_smem with packed weights, converted block by block.
+template <int NM, int S>
+MOE_DEVFN void row_dot_smem_packed(uint32_t row, int K, const uint4 (&wr)[NM][S], const float (&ws)[NM][S],
+                                   float (&acc)[NM]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int b = lane + 32 * s;
+    if (b < nb) {
+      const uint4 lo = lds128(row + 16u * b), hi = lds128(row + 16u * (nb + b));
+      const float sx = lds_f32(row + (uint32_t)K + 4u * b);
+      const int xsum = lds_s32(row + (uint32_t)K + 4u * (nb + b));
+      const uint32_t xw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        uint32_t q[8];
+        e2m1x8_to_off12(wr[m][s].x, q[0], q[1]);
+        e2m1x8_to_off12(wr[m][s].y, q[2], q[3]);
+        e2m1x8_to_off12(wr[m][s].z, q[4], q[5]);
+        e2m1x8_to_off12(wr[m][s].w, q[6], q[7]);
+        int d = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d = __dp4a((int)xw[j], (int)q[j], d);
+        const int I = d - 12 * xsum;
+        acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, ws[m][s]), acc[m]);
+      }
+    }
+  }
+}
+
+// 8 E2M1 codes -> twice their magnitudes, split by sign: pos holds 2|v| for
+// positive codes and 0 for negative ones, neg the reverse, so that
+// dot(x, 2v) = dot(x, pos) - dot(x, neg).  One byte-permute lookup per 4
+// codes and sign (a set selector top bit replicates the table byte's zero sign
+// bit); the high halves come down with umulhi, which runs on the multiply
+// pipe instead of the integer-logic pipe.  For weights used by one row.
+MOE_DEVFN void e2m1x8_pos_neg(uint32_t w, uint32_t &p_lo, uint32_t &p_hi, uint32_t &n_lo, uint32_t &n_hi) {
+  const uint32_t T0 = 0x03020100u, T1 = 0x0C080604u;  // {0,1,2,3 | 4,6,8,12}
+  const uint32_t wx = w ^ 0x88888888u;
+  p_lo = prmt(T0, T1, w);
+  p_hi = prmt(T0, T1, __umulhi(w, 0x10000u));
+  n_lo = prmt(T0, T1, wx);
+  n_hi = prmt(T0, T1, __umulhi(wx, 0x10000u));
+}
+
+// row_dot_smem with packed weights decoded by sign (no block sums needed).
+// The integer block dots, and so every result, equal row_dot_smem's.
+template <int NM, int S>
+MOE_DEVFN void row_dot_smem_pn(uint32_t row, int K, const uint4 (&wr)[NM][S], const float (&ws)[NM][S],
+                               float (&acc)[NM]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int b = lane + 32 * s;
+    if (b < nb) {
+      const uint4 lo = lds128(row + 16u * b), hi = lds128(row + 16u * (nb + b));
+      const float sx = lds_f32(row + (uint32_t)K + 4u * b);
+      const uint32_t xw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        const uint32_t wv[4] = {wr[m][s].x, wr[m][s].y, wr[m][s].z, wr[m][s].w};
+        int dp = 0, dn = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t pl, ph, nl, nh;
+          e2m1x8_pos_neg(wv[j], pl, ph, nl, nh);
+          dp = __dp4a((int)xw[2 * j], (int)pl, dp);
+          dp = __dp4a((int)xw[2 * j + 1], (int)ph, dp);
+          dn = __dp4a((int)xw[2 * j], (int)nl, dn);
+          dn = __dp4a((int)xw[2 * j + 1], (int)nh, dn);
+        }
+        acc[m] = __fmaf_rn(__int2float_rn(dp - dn), __fmul_rn(sx, ws[m][s]), acc[m]);
+      }
+    }
+  }
+}
+
+// The same from a row of codes and scales in global memory.
+template <int NM, int S>
+MOE_DEVFN void row_dot_global(const int8_t *xr, const float *sr, int K, const uint32_t (&wq)[NM][S][8],
+                              const float (&ws)[NM][S], float (&acc)[NM]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int b = lane + 32 * s;
+    if (b < nb) {
+      const uint4 lo = ldg_nc(xr + 32 * b), hi = ldg_nc(xr + 32 * b + 16);
+      block_terms<NM, S>(s, lo, hi, sr[b], block_sum8(lo, hi), wq, ws, acc);
+    }
+  }
+}
+
+// Butterfly of two per-lane sums at once: lanes 0-15 finish the first, 16-31
+// the second, each with exactly the pairs and association of its own full
+// xor butterfly (so the bits equal two separate butterflies).  Lane 0 returns
+// (first, second).
+MOE_DEVFN void reduce_pair(float a, float b, float &first, float &second) {
+  const int lane = threadIdx.x & 31;
+  const bool upper = (lane & 16) != 0;
+  float keep = upper ? b : a;
+  const float send = upper ? a : b;
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, o));
+  first = keep;
+  second = __shfl_xor_sync(0xffffffffu, keep, 16);
+}
+
+MOE_DEVFN float reduce_one(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Loads that bypass L1 (data written by other CTAs of the same grid).
+MOE_DEVFN float ldcg_f32(const float *p) {
+  float r;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+MOE_DEVFN uint4 ldcg_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// Stage one activation row from global Q8 codes + scales into the shared
+// layout above, computing the block sums.  Lanes of the calling threads take
+// blocks idx0, idx0+stride, ...
+MOE_DEVFN void stage_q8_block(uint32_t row, int K, int b, const int8_t *src_codes, float scale) {
+  const int nb = K / 32;
+  const uint4 lo = ldg_nc(src_codes + 32 * b), hi = ldg_nc(src_codes + 32 * b + 16);
+  sts128(row + 16u * b, lo);
+  sts128(row + 16u * (nb + b), hi);
+  sts32(row + (uint32_t)K + 4u * b, __float_as_uint(scale));
+  sts32(row + (uint32_t)K + 4u * (nb + b), (uint32_t)block_sum8(lo, hi));
+}
+
+}  // namespace moe

@@ -23,7 +23,7 @@
 // lane sums are combined by a fixed xor butterfly.  Nothing depends on how
 // many rows the call has, so a T-row call reproduces T one-row calls bit for
 // bit.
-#include "common.cuh"
+#include "mx_device.cuh"
 
 namespace moe {
 namespace {
@@ -43,6 +43,8 @@ struct MxArgs {
   int A, k, E;
   int K;  // reduction length
   int N;  // output rows per expert
+  int n_act;          // activation rows: T (gate/up) or A (down)
+  uint32_t kdiv;      // ceil(2^32 / k): token of assignment a = umulhi(a, kdiv)
   float *out0, *out1;
   int64_t ld_out;
   int R;              // output rows per CTA (max)
@@ -51,11 +53,21 @@ struct MxArgs {
   uint32_t wreg;      // bytes of one matrix's weight slice region in a stage
   uint32_t sreg;      // bytes of one matrix's scale slice region (16-aligned)
   int scale16;        // scale rows are whole 16-byte chunks at 16-byte aligned addresses
+  int rowtab;         // sorted positions (<= kRowTab) get their activation row from shared memory
+  int act_smem;       // all activation rows are staged in shared memory
+  uint32_t act_row_bytes;  // K codes (two half-block planes) + nb scales + nb block sums
   unsigned *status;
 };
 
-MOE_DEVFN float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+constexpr int kRowTab = 4096;
 
+// Shared-memory layout (dynamic):
+//   [nstage weight stages][full bars][empty bars][active: E][offs: E+1]
+//   [rowtab: kRowTab ints, if used][activation rows, if staged]
+// An activation row holds the K Q8 codes as two planes of 16-byte half
+// blocks (first halves of all blocks, then second halves: lanes reading
+// consecutive blocks hit consecutive 16-byte bank groups), then nb fp32
+// scales, then nb int32 block sums.
 template <int MODE, int S>
 __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   constexpr int NM = (MODE == kDown) ? 1 : 2;
@@ -75,6 +87,10 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   uint64_t *empty = full + nstage;
   int *active = reinterpret_cast<int *>(empty + nstage);  // [E] active experts, in id order
   int *offs = active + p.E;                               // [E+1] copy of offsets
+  int *rowtab = offs + p.E + 1;                           // [kRowTab] activation row per sorted position
+  uint8_t *act = reinterpret_cast<uint8_t *>(rowtab + (p.rowtab ? kRowTab : 0));
+  act = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(act) + 15) & ~uintptr_t(15));
+  const uint32_t act_base = smem_addr(act);
 
   // Stage the expert offsets in one parallel pass, then list the experts
   // that own rows (ballot compaction keeps increasing id order).
@@ -92,15 +108,15 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
     const unsigned lt = (1u << lane) - 1u;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + lane;
-      bool act = false;
+      bool act_e = false;
       if (e < p.E) {
         const int64_t b = offs[e], en = offs[e + 1];
         const bool bad = b < 0 || en < b || en > p.cap;
         if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-        act = !bad && en > b;
+        act_e = !bad && en > b;
       }
-      const unsigned m = __ballot_sync(0xffffffffu, act);
-      if (act) active[cnt + __popc(m & lt)] = e;
+      const unsigned m = __ballot_sync(0xffffffffu, act_e);
+      if (act_e) active[cnt + __popc(m & lt)] = e;
       cnt += __popc(m);
     }
     if (lane == 0) n_active = cnt;
@@ -147,6 +163,25 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   }
 
   // -------------------------------------------------------------- consumers
+  // Activation row of each sorted position (-1: padding, -2: out of range).
+  const int nsorted = offs[p.E] < 0 ? 0 : (offs[p.E] > p.cap ? (int)p.cap : offs[p.E]);
+  if (p.rowtab) {
+    for (int q = tid; q < nsorted; q += ncons * 32) {
+      const int a = p.sorted[q];
+      rowtab[q] = a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : (int)__umulhi((unsigned)a, p.kdiv)));
+    }
+  }
+  // Stage every activation row once: codes in two half-block planes, the
+  // scales, and the exact block sums sum(q) used by the offset encoding.
+  if (p.act_smem) {
+    for (int idx = tid; idx < p.n_act * nb; idx += ncons * 32) {
+      const int r = idx / nb, b = idx - r * nb;
+      stage_q8_block(act_base + (uint32_t)r * p.act_row_bytes, p.K, b, p.aq + (int64_t)r * p.ld_aq,
+                     p.as[(int64_t)r * p.ld_as + b]);
+    }
+  }
+  bar_sync_named(1, ncons * 32);
+
   for (int it = 0; it < nact; ++it) {
     const int st = it % nstage;
     if (!mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status)) break;
@@ -157,66 +192,44 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
     for (int r = warp; r < R; r += ncons) {
       uint32_t wq[NM][S][8];
       float ws[NM][S];
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-          const int b = lane + 32 * s;
-          if (b < nb) {
-            const uint4 raw = lds128(sbase + m * p.wreg + (uint32_t)r * (p.K / 2) + 16u * b);
-            e2m1x8_to_off12(raw.x, wq[m][s][0], wq[m][s][1]);
-            e2m1x8_to_off12(raw.y, wq[m][s][2], wq[m][s][3]);
-            e2m1x8_to_off12(raw.z, wq[m][s][4], wq[m][s][5]);
-            e2m1x8_to_off12(raw.w, wq[m][s][6], wq[m][s][7]);
-            ws[m][s] = e8m0_half(lds_u8(sbase + NM * p.wreg + m * p.sreg + (uint32_t)r * nb + b));
-          }
-        }
-      }
+      load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
       const int n = n0 + r;
 #pragma unroll 1
       for (int q = seg_b; q < seg_e; ++q) {
-        const int a = p.sorted[q];
-        if (a < 0) continue;
-        if (a >= p.A) {
-          if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-          continue;
+        int a, arow;
+        if (p.rowtab && q < kRowTab) {
+          arow = rowtab[q];
+          if (arow < 0) {
+            if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+            continue;
+          }
+          a = p.sorted[q];
+        } else {
+          a = p.sorted[q];
+          if (a < 0) continue;
+          if (a >= p.A) {
+            if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+            continue;
+          }
+          arow = MODE == kDown ? a : (int)__umulhi((unsigned)a, p.kdiv);
         }
-        const int64_t arow = (MODE == kDown) ? a : a / p.k;
-        const int8_t *xr = p.aq + arow * p.ld_aq;
-        const float *sr = p.as + arow * p.ld_as;
         float acc[NM];
-#pragma unroll
-        for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-          const int b = lane + 32 * s;
-          if (b < nb) {
-            const uint4 x0 = ldg_nc(xr + 32 * b), x1 = ldg_nc(xr + 32 * b + 16);
-            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float sx = sr[b];
-            int xsum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) xsum = __dp4a((int)xw[j], 0x01010101, xsum);
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              int d = 0;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) d = __dp4a((int)xw[j], (int)wq[m][s][j], d);
-              const int I = d - 12 * xsum;
-              acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, ws[m][s]), acc[m]);
+        if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+        else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+        if (NM == 2) {
+          float g, u;
+          reduce_pair(acc[0], acc[NM - 1], g, u);
+          if (lane == 0) {
+            if (MODE == kGateUpSwiglu) {
+              p.out0[(int64_t)a * p.ld_out + n] = __fmul_rn(silu(g), u);
+            } else {
+              p.out0[(int64_t)a * p.ld_out + n] = g;
+              p.out1[(int64_t)a * p.ld_out + n] = u;
             }
           }
-        }
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xffffffffu, acc[m], o));
-        }
-        if (lane == 0) {
-          float *dst = p.out0 + (int64_t)a * p.ld_out + n;
-          if (MODE == kGateUpSwiglu) *dst = __fmul_rn(silu(acc[0]), acc[NM - 1]);
-          else *dst = acc[0];
-          if (MODE == kGateUpRaw) p.out1[(int64_t)a * p.ld_out + n] = acc[NM - 1];
+        } else {
+          const float v = reduce_one(acc[0]);
+          if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
         }
       }
     }
@@ -236,35 +249,37 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   int smem_optin = 0;
   err = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return cuda_fail(err, name);
+  const size_t budget = (size_t)smem_optin - 1024;
   const int sms = sm_count();
-  const size_t extra = (size_t)p.E * 8 + 4 + 16 * 8 + 256;
+  p.rowtab = p.cap <= kRowTab ? 1 : 0;
+  p.act_row_bytes = (uint32_t)p.K + 8u * nb;
+  const size_t fixed = (size_t)p.E * 8 + 4 + 16 * 8 + 32 + (p.rowtab ? 4 * kRowTab : 0);
   int G = p.N < sms ? p.N : sms;
   for (;;) {
     p.R = (p.N + G - 1) / G;
     p.wreg = (uint32_t)p.R * (p.K / 2);
     p.sreg = ((uint32_t)p.R * nb + 15u) & ~15u;
     p.stage_bytes = (NM * (p.wreg + p.sreg) + 127u) & ~127u;
-    const size_t avail = (size_t)smem_optin - 1024 - extra;
-    int ns = (int)(avail / p.stage_bytes);
-    if (ns > 8) ns = 8;
-    if (ns >= 2 || G >= p.N) {
-      p.nstage = ns;
-      break;
-    }
+    if (budget >= fixed + 2 * (size_t)p.stage_bytes || G >= p.N) break;
     G = (2 * G < p.N) ? 2 * G : p.N;
   }
+  const size_t act_bytes = (size_t)p.n_act * p.act_row_bytes + 16;
+  p.act_smem = budget >= fixed + 2 * (size_t)p.stage_bytes + act_bytes ? 1 : 0;
+  const size_t avail = budget - fixed - (p.act_smem ? act_bytes : 0);
+  int ns = (int)(avail / p.stage_bytes);
+  p.nstage = ns > 6 ? 6 : ns;
   if (p.nstage < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
   p.scale16 = (nb % 16) == 0 && (uintptr_t)p.s0 % 16 == 0 && (p.s1 == nullptr || (uintptr_t)p.s1 % 16 == 0);
-  int per_warp = (p.R + 14) / 15;
-  int ncons = (p.R + per_warp - 1) / per_warp;
-  const size_t smem = (size_t)p.nstage * p.stage_bytes + 2 * 8 * (size_t)p.nstage + (size_t)p.E * 8 + 4;
+  const int per_warp = (p.R + 14) / 15;
+  const int ncons = (p.R + per_warp - 1) / per_warp;
+  const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + (p.act_smem ? act_bytes : 0);
   const dim3 block((ncons + 1) * 32);
 
   static bool configured[3][3][64] = {};
   const int si = S == 1 ? 0 : (S == 2 ? 1 : 2);
   auto kern = S == 1 ? mx_expert_kernel<MODE, 1> : (S == 2 ? mx_expert_kernel<MODE, 2> : mx_expert_kernel<MODE, 4>);
   if (dev < 64 && !configured[MODE][si][dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin - 1024);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
     if (err != cudaSuccess) return cuda_fail(err, name);
     configured[MODE][si][dev] = true;
   }
@@ -316,6 +331,8 @@ static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const f
   p.w0 = wg; p.s0 = sg; p.w1 = wu; p.s1 = su;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
   p.A = T * k; p.k = k; p.E = E; p.K = H; p.N = I;
+  p.n_act = T;
+  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
   p.out0 = o0; p.out1 = o1; p.ld_out = ld;
   p.status = device_status_word();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -353,6 +370,8 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
   p.w0 = wd; p.s0 = sd;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
   p.A = T * k; p.k = k; p.E = E; p.K = I; p.N = H;
+  p.n_act = T * k;
+  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
   p.out0 = y; p.ld_out = ld_y;
   p.status = device_status_word();
   return launch_mx<kDown>(p, static_cast<cudaStream_t>(stream), name);

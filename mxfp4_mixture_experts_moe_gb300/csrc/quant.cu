@@ -5,7 +5,7 @@
 // values/scales").  scale = amax/127 (IEEE division), q = rne(x * (1/scale))
 // clamped to [-127, 127]; every step is an IEEE-rounded fp32 operation, so the
 // codes are the same bits on any IEEE machine.
-#include "common.cuh"
+#include "mx_device.cuh"
 
 namespace moe {
 namespace {
@@ -41,23 +41,8 @@ quant_q8_kernel(const void *x, int64_t ld_x, int rows, int nblk, int8_t *q, int6
       v[4 * c + 3] = __uint_as_float(w.w);
     }
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int l = 0; l < 32; ++l) amax = fmaxf(amax, fabsf(v[l]));
-  const float d = __fdiv_rn(amax, 127.0f);
-  const float inv = d > 0.0f ? __frcp_rn(d) : 0.0f;
   uint32_t packed[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int qi = __float2int_rn(__fmul_rn(v[4 * c + j], inv));
-      qi = max(-127, min(127, qi));
-      word |= (uint32_t)(qi & 0xFF) << (8 * j);
-    }
-    packed[c] = word;
-  }
+  const float d = q8_block(v, packed, nullptr);
   uint4 *dst = reinterpret_cast<uint4 *>(q + r * ld_q + 32 * b);
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);

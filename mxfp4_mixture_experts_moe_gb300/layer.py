@@ -11,8 +11,8 @@ import dataclasses
 
 import torch
 
-from . import (act_quant_q8, moe_combine, moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk,
-               moe_sort_tokens, moe_sort_tokens_capacity)
+from . import (act_quant_q8, moe_combine, moe_decode_forward, moe_decode_max_tokens, moe_decode_workspace_bytes,
+               moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens, moe_sort_tokens_capacity)
 
 
 @dataclasses.dataclass
@@ -65,7 +65,7 @@ class Workspace:
             return full[:, :cols]
 
         self.T, self.A, self.tile_rows = T, A, tile_rows
-        self.logits = buf(T, E, torch.float32)
+        self.logits = torch.empty(T, E, dtype=torch.float32, device=device)  # [T][E], no row stride in the ABI
         self.ids = torch.empty(T, k, dtype=torch.int32, device=device)
         self.w = torch.empty(T, k, dtype=torch.float32, device=device)
         self.offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
@@ -79,11 +79,28 @@ class Workspace:
         self.hs = buf(A, I // 32, torch.float32)
         self.y = buf(A, H, torch.float32)
         self.out = buf(T, H, torch.float32)
+        # grid-barrier counters of the fused decode path (zero-filled once)
+        nws = (moe_decode_workspace_bytes() + 7) // 8
+        self.decode_ws = torch.zeros(nws, dtype=torch.int64, device=device)
 
 
 class MoeLayer:
-    def __init__(self, weights: LayerWeights):
+    def __init__(self, weights: LayerWeights, fused: bool | None = None):
+        """fused: None = use the single-launch decode path when the batch
+        allows it; True / False force it on / off."""
         self.lw = weights
+        self.fused = fused
+
+    def use_fused(self, T: int) -> bool:
+        """The single-launch path takes batches up to moe_decode_max_tokens()
+        (activation rows must fit its shared memory); larger ones use the
+        stage calls."""
+        if self.fused is False:
+            return False
+        if not hasattr(self, "_max_t"):
+            lw = self.lw
+            self._max_t = moe_decode_max_tokens(lw.H, lw.E, lw.k, lw.I)
+        return 0 < T <= self._max_t
 
     def forward(self, x: torch.Tensor, ws: Workspace, stream=None, events: dict | None = None) -> torch.Tensor:
         """out = MoE(x) for the T rows of x ([T, H] bf16/f32, unit column stride).
@@ -94,6 +111,14 @@ class MoeLayer:
         lw = self.lw
         s = torch.cuda.current_stream() if stream is None else stream
         ev = events or {}
+        if self.use_fused(ws.T):
+            if "decode" in ev:
+                ev["decode"][0].record(s)
+            moe_decode_forward(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, lw.k, ws.out, ws.logits,
+                               ws.ids, ws.w, ws.h, ws.y, ws.decode_ws, stream=s)
+            if "decode" in ev:
+                ev["decode"][1].record(s)
+            return ws.out
 
         def stage(name, fn, *args):
             if name in ev:
@@ -112,5 +137,6 @@ class MoeLayer:
         stage("combine", moe_combine, ws.y, ws.w, ws.out)
         return ws.out
 
-    # launches per forward, for launch accounting
-    KERNELS_PER_FORWARD = 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
+    def kernels_per_forward(self, T: int) -> int:
+        """Launches of this library's kernels per forward."""
+        return 1 if self.use_fused(T) else 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine

@@ -53,9 +53,11 @@ def _oracle_experts(spec, ids):
     return out
 
 
-def _run(moe, lw, x_dev, pad=0, tile_rows=1):
+def _run(moe, lw, x_dev, pad=0, tile_rows=1, fused=None):
+    """fused=None: the library's choice (the single-launch path for small
+    batches); False: the six stage calls (which expose every intermediate)."""
     ws = moe.Workspace(x_dev.shape[0], lw, "cuda", pad=pad, tile_rows=tile_rows)
-    out = moe.MoeLayer(lw).forward(x_dev, ws)
+    out = moe.MoeLayer(lw, fused=fused).forward(x_dev, ws)
     torch.cuda.synchronize()
     return ws, host(out)
 
@@ -106,7 +108,7 @@ def test_tiny_layer(moe):
     lw = upload_layer(spec)
     for T in (1, 3, 16):
         x = synth.activations(spec, T)
-        ws, out = _run(moe, lw, dev(x))
+        ws, out = _run(moe, lw, dev(x), fused=False)
         _check_vs_oracle(spec, x, ws, out)
     assert moe.moe_device_status() == 0
 
@@ -115,7 +117,7 @@ def test_tiny_layer(moe):
 def test_dsv4_decode_vs_oracle(moe, dsv4, T):
     spec = synth.DSV4
     x = synth.activations(spec, T, token0=100)
-    ws, out = _run(moe, dsv4, dev(x))
+    ws, out = _run(moe, dsv4, dev(x), fused=False)
     stats = _check_vs_oracle(spec, x, ws, out)
     print(f"T={T}: {stats}")
     assert moe.moe_device_status() == 0
@@ -123,7 +125,8 @@ def test_dsv4_decode_vs_oracle(moe, dsv4, T):
 
 def test_exact_rows_1_to_16(moe, dsv4):
     """Every row of a 2..16-row call equals its one-row call bit for bit, with
-    tight and padded strides."""
+    tight and padded strides, across code paths: one-row calls take the fused
+    single-launch path, 2..10 rows too, 16 rows the stage calls."""
     spec = synth.DSV4
     x = synth.activations(spec, 16, token0=500)
     singles = [_run(moe, dsv4, dev(x[t:t + 1]))[1] for t in range(16)]
@@ -145,6 +148,7 @@ def test_exact_rows_graph_replay(moe, dsv4):
     ws = moe.Workspace(1, dsv4, "cuda")
     layer = moe.MoeLayer(dsv4)
     s = torch.cuda.Stream()
+    torch.cuda.synchronize()  # buffers were filled on the default stream
     with torch.cuda.stream(s):
         layer.forward(x, ws, s)
     torch.cuda.synchronize()
@@ -163,7 +167,7 @@ def test_zipf_batches(moe, dsv4_zipf):
     spec = synth.DSV4_ZIPF
     for T in (32, 64):
         x = synth.activations(spec, T, token0=2000)
-        ws, out = _run(moe, dsv4_zipf, dev(x))
+        ws, out = _run(moe, dsv4_zipf, dev(x), fused=False)
         ids = host(ws.ids)
         assert len(np.unique(ids)) < 0.9 * min(256, T * 6)  # skewed routing reuses experts
         _check_vs_oracle(spec, x, ws, out, sample=[0, 5, T - 1])
@@ -177,7 +181,7 @@ def test_zipf_batches(moe, dsv4_zipf):
 def test_prefill_chunks(moe, dsv4, T, sample):
     spec = synth.DSV4
     x = synth.activations(spec, T, token0=10000)
-    ws, out = _run(moe, dsv4, dev(x), tile_rows=1)
+    ws, out = _run(moe, dsv4, dev(x), tile_rows=1, fused=False)
     _check_vs_oracle(spec, x, ws, out, sample=sample)
     for t in sample[:2]:
         _, o1 = _run(moe, dsv4, dev(x[t:t + 1]))
@@ -192,5 +196,8 @@ def test_full_decode_only_selected_experts_read(moe):
     x = synth.activations(spec, 1, token0=31)
     _, ids, _ = oracle.route(x, synth.router_weights(spec), spec.k)
     lw = upload_layer(spec, only=set(ids.ravel().tolist()))
-    ws, out = _run(moe, lw, dev(x))
+    ws, out = _run(moe, lw, dev(x), fused=False)
     _check_vs_oracle(spec, x, ws, out)
+    ws, out = _run(moe, lw, dev(x), fused=True)
+    assert max_err_over_rms(out, oracle.layer(x, synth.router_weights(spec), None, spec.k,
+                                              _oracle_experts(spec, ids))["out"]) <= TOL
