@@ -247,6 +247,31 @@ MOE_API moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t 
                                       float *h, int64_t ld_h, float *y, int64_t ld_y,
                                       void *workspace, size_t ws_bytes, void *stream);
 
+/* moe_decode_forward for callers that cannot allocate device memory when they
+ * run the layer (serving loops that cannot afford the device-wide
+ * synchronisation an allocation can cause, runtimes that own all device
+ * memory, embedders that forbid allocation after start-up).  The papers have no counterpart to this call;
+ * it exists for such callers only.
+ * Same inputs, rules and output `out` as moe_decode_forward, computed by the
+ * same kernel with the same bits.  Every intermediate (barrier counters,
+ * logits, ids, weights, h) lives in one fixed array of device memory owned by
+ * the library (about 1.1 MiB per device, held from library load until process
+ * exit); nothing is allocated and the intermediates are not returned.
+ * Limits of that array: T*k <= 64, T*E <= 32768, I <= 4096; beyond them the
+ * call returns MOE_ERR_UNSUPPORTED (use moe_decode_forward with your own
+ * buffers).
+ * The first call on a device looks up the array's device address (set-up);
+ * make that first call before any stream capture.  Each call clears the
+ * barrier words on `stream` before its launch.  All calls on one device share
+ * the array: calls that may overlap on the GPU (different streams without
+ * ordering between them) race and give wrong results. */
+MOE_API moe_status moe_decode_forward_noalloc(const void *x, moe_dtype x_dtype, int64_t ld_x,
+                                              const void *w_router, moe_dtype w_dtype, const float *bias,
+                                              const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
+                                              const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
+                                              int T, int H, int E, int k, int I,
+                                              float *out, int64_t ld_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
            "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_decode_workspace_bytes",
-           "moe_decode_max_tokens", "moe_decode_forward"]
+           "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc"]
 
 _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 _SIG = {
@@ -47,6 +47,7 @@ _SIG = {
     "moe_decode_max_tokens": (_I, [_I, _I, _I, _I]),
     "moe_decode_forward": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L] + [_P] * 3
                            + [_P, _L, _P, _L, _P, C.c_size_t, _P]),
+    "moe_decode_forward_noalloc": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L, _P]),
 }
 library_path = _LIB_PATH
 
@@ -200,6 +201,21 @@ def moe_decode_forward(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out, logits
                                    _ptr(out), _ld(out), _ptr(logits), _ptr(ids), _ptr(weights), _ptr(h), _ld(h),
                                    _ptr(y), _ld(y) if y is not None else 0, _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_decode_forward_noalloc(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out, stream=None):
+    """moe_decode_forward for callers that cannot allocate device memory when
+    they run the layer (a runtime that owns all device memory, an embedder
+    that forbids allocation after start-up): the intermediates live in a
+    fixed device array owned by the library (T*k <= 64, T*E <= 32768,
+    I <= 4096) and only ``out`` is written.  The first call on a device looks
+    up that array; make it before any stream capture.  Calls that overlap on
+    the GPU share the array and race."""
+    T, H = x.shape[0], w_router.shape[1]
+    E, I = w_router.shape[0], wg.shape[1]
+    _check(_lib.moe_decode_forward_noalloc(_ptr(x), _dt(x), _ld(x), _ptr(w_router), _dt(w_router), _ptr(bias),
+                                           _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(wd), _ptr(sd), T, H, E, k,
+                                           I, _ptr(out), _ld(out), _stream(stream)))
 
 
 from .layer import MoeLayer, LayerWeights, Workspace  # noqa: E402
