@@ -232,8 +232,8 @@ MOE_API int moe_decode_max_tokens(int H, int E, int k, int I);
  *           Calls that share a workspace must not run concurrently.
  * Requires T <= moe_decode_max_tokens(H, E, k, I) (T*k <= 64, T <= 14, and the
  * activation rows must fit shared memory; else MOE_ERR_UNSUPPORTED: use the
- * stage calls), plus the stage calls' shape rules (H, I multiples of 128,
- * <= 4096).
+ * stage calls), E <= 256, plus the stage calls' shape rules (H, I multiples
+ * of 128, <= 4096).
  * A wait that does not complete (a device fault elsewhere) sets
  * MOE_DEV_WAIT_TIMEOUT and the launch returns with outputs incomplete; the
  * workspace must then be zero-filled again. */

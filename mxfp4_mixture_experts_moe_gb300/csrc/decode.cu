@@ -155,35 +155,54 @@ MOE_DEVFN void load32_smem(uint32_t addr, bool bf16, float (&v)[32]) {
   }
 }
 
-// router_logits_warp with the router row and the activation rows in shared
-// memory: the same chunk ownership, fma order and butterfly.
-MOE_DEVFN void router_logits_smem(uint32_t wrow, bool wbf, uint32_t x0, uint32_t xrow_bytes, bool xbf, int nt, int H,
-                                  float (&p)[8]) {
+// One router logit (one expert row, one token) from shared memory, one warp,
+// in the order of router_logits_warp: lane l accumulates the chunks l, l+32,
+// ... of 8 consecutive inputs in increasing order with one fma per element,
+// then the 32 partial sums meet in an xor butterfly.  The chunk loads of four
+// consecutive passes are issued together; the fma order is unchanged.
+MOE_DEVFN float router_dot_smem(uint32_t wrow, bool wbf, uint32_t xrow, bool xbf, int H) {
   const int lane = threadIdx.x & 31;
   const int nch = H / 8;
-  const uint32_t wstep = wbf ? 16u : 32u, xstep = xbf ? 16u : 32u;
+  float p = 0.0f;
+  if (wbf && xbf) {
+    // bf16 rows: the raw 16-byte chunks of four passes in flight, widened on use
+#pragma unroll 1
+    for (int c0 = lane; c0 < nch; c0 += 128) {
+      uint4 wr[4], xr[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) p[j] = 0.0f;
-  for (int c = lane; c < nch; c += 32) {
-    float wv[8];
-    load8_smem(wrow + (uint32_t)c * wstep, wbf, wv);
+      for (int i = 0; i < 4; ++i) {
+        if (c0 + 32 * i < nch) {
+          wr[i] = lds128(wrow + 16u * (uint32_t)(c0 + 32 * i));
+          xr[i] = lds128(xrow + 16u * (uint32_t)(c0 + 32 * i));
+        }
+      }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < nt) {
-        float xv[8];
-        load8_smem(x0 + (uint32_t)j * xrow_bytes + (uint32_t)c * xstep, xbf, xv);
+      for (int i = 0; i < 4; ++i) {
+        if (c0 + 32 * i < nch) {
+          const uint32_t wv[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+          const uint32_t xv[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) p[j] = __fmaf_rn(xv[q], wv[q], p[j]);
+          for (int q = 0; q < 4; ++q) {
+            p = __fmaf_rn(bf16_lo(xv[q]), bf16_lo(wv[q]), p);
+            p = __fmaf_rn(bf16_hi(xv[q]), bf16_hi(wv[q]), p);
+          }
+        }
       }
     }
-  }
+  } else {
+    const uint32_t wstep = wbf ? 16u : 32u, xstep = xbf ? 16u : 32u;
+#pragma unroll 1
+    for (int c = lane; c < nch; c += 32) {
+      float wv[8], xv[8];
+      load8_smem(wrow + (uint32_t)c * wstep, wbf, wv);
+      load8_smem(xrow + (uint32_t)c * xstep, xbf, xv);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < nt) {
-#pragma unroll
-      for (int s = 16; s >= 1; s >>= 1) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], s));
+      for (int q = 0; q < 8; ++q) p = __fmaf_rn(xv[q], wv[q], p);
     }
   }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, s));
+  return p;
 }
 
 // Q8 of one 32-value block into a staged row (split-half layout with the
@@ -344,21 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const unsigned long long base = bar_base;
 
   // ---------------------------------------------------------------- A
-  if (warp < nrw) {
-    const int e = cta + G * warp;
-    if (e < E) {
-      for (int t0 = 0; t0 < T; t0 += 8) {
-        const int nt = min(8, T - t0);
-        float pl[8];
-        router_logits_smem(front + (uint32_t)warp * H * wsz, p.wbf != 0, xs_smem + (uint32_t)t0 * H * xsz, H * xsz,
-                           p.xbf != 0, nt, H, pl);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (lane == 0 && j < nt) p.logits[(int64_t)(t0 + j) * E + e] = pl[j];
-      }
+  // router: one warp per (router row of this CTA, token); Q8(x) on the rest
+  int nrows_here = 0;
+  for (int w = 0; w < nrw; ++w) nrows_here += (cta + G * w) < E;
+  const int nunits = nrows_here * T;
+  const int rwarps = min(nunits, kWarps / 2);
+  if (warp < rwarps) {
+#pragma unroll 1
+    for (int u = warp; u < nunits; u += rwarps) {
+      const int w = u / T, t = u - w * T;
+      const float v = router_dot_smem(front + (uint32_t)w * H * wsz, p.wbf != 0, xs_smem + (uint32_t)t * H * xsz,
+                                      p.xbf != 0, H);
+      if (lane == 0) p.logits[(int64_t)t * E + cta + G * w] = v;
     }
   } else {
-    const int q0 = tid - nrw * 32, qn = kThreads - nrw * 32;
+    const int q0 = tid - rwarps * 32, qn = kThreads - rwarps * 32;
     for (int idx = q0; idx < T * nbH; idx += qn) {
       const int t = idx / nbH, b = idx - t * nbH;
       float v[32];
@@ -374,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   if (warp < T) {
     int id[8];
     float wv[8];
-    topk_warp(logit_s + warp * E, p.bias, E, k, id, wv);
+    topk_warp_s<8>(logit_s + warp * E, p.bias, E, k, id, wv);  // E <= 256 on this path
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k && lane == j) {
@@ -609,7 +628,7 @@ using namespace moe;
 extern "C" size_t moe_decode_workspace_bytes(void) { return 64; }  // [0] counter, [1] hold, spare
 
 extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) {
-  if (H <= 0 || E <= 0 || k <= 0 || k > 8 || I <= 0 || H % 128 || I % 128 || H > 4096 || I > 4096 || E > 1024) return 0;
+  if (H <= 0 || E <= 0 || k <= 0 || k > 8 || I <= 0 || H % 128 || I % 128 || H > 4096 || I > 4096 || E > 256) return 0;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
@@ -639,7 +658,7 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   if (w_dtype != MOE_F32 && w_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad router dtype", name);
   if (H % 128 || I % 128) return fail(MOE_ERR_INVALID_ARG, "%s: H=%d and I=%d must be multiples of 128", name, H, I);
   if (H > 4096 || I > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: H, I <= 4096", name);
-  if (E > 1024) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d > 1024", name, E);
+  if (E > 256) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d > 256 (use the stage calls)", name, E);
   if (k > 8 || k > E) return fail(MOE_ERR_INVALID_ARG, "%s: k=%d must be <= min(E, 8)", name, k);
   if (T == 0) return MOE_OK;
   const int A = T * k;

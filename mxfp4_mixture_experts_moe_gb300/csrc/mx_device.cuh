@@ -92,54 +92,70 @@ MOE_DEVFN void router_logits_warp(const void *x, bool xbf, int64_t ld_x, const v
   }
 }
 
-MOE_DEVFN bool topk_better(float s, int i, float bs, int bi) { return s > bs || (s == bs && i < bi); }
-
-// Top-k of one token, one warp: k rounds of an xor-butterfly argmax over
-// (score desc, id asc); score = logit (+ bias), re-read each round.  Weights:
-// sigmoid of the selected scores over their sum.  Every lane returns the same
-// ids/weights.
+// Top-k of one token, one warp.  score = logit (+ bias); the k largest
+// scores are taken in descending order, equal scores by lower expert id, and
+// a NaN score is never taken (an id of 0x7fffffff marks a slot that only NaN
+// scores were left for).  Weights: sigmoid of the selected scores over their
+// sum, added in slot order.  Every lane returns the same ids/weights.
 MOE_DEVFN float topk_score(const float *logits_row, const float *bias, int e) {
   const float v = logits_row[e];
   return bias ? __fadd_rn(v, bias[e]) : v;
 }
 
-// Order-preserving key of a float score (larger score -> larger key); -0 is
-// first turned into +0 so that the keys tie exactly where the scores compare
-// equal.
+// Order-preserving key of a float score (larger score -> larger key, every
+// real score > 0); -0 is first turned into +0 so that the keys tie exactly
+// where the scores compare equal.  NaN gets key 0, "absent".
 MOE_DEVFN uint32_t score_key(float v) {
+  if (v != v) return 0u;
   const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+MOE_DEVFN float key_score(uint32_t key) {  // inverse of score_key on real scores
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
 
-MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
+// S = scores per lane (expert lane + 32 s); E <= 32 * S.  Each lane reads its
+// scores once, then every round is register work: the lane's best key (the
+// first of equal keys has the lower id), the warp's largest key, and the
+// lowest id holding it.
+template <int S>
+MOE_DEVFN void topk_warp_s(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;  // bit s: expert lane + 32 s already selected
+  uint32_t key[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int e = lane + 32 * s;
+    key[s] = e < E ? score_key(topk_score(logits_row, bias, e)) : 0u;
+  }
   float sel[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     ids[j] = 0;
     sel[j] = 0.0f;
-    if (j < k) {
-      // this lane's best unselected expert (score desc, id asc) ...
-      float bs = -CUDART_INF_F;
-      int bi = 0x7fffffff;
-      for (int s = 0, e = lane; e < E; ++s, e += 32) {
-        if ((taken >> s) & 1u) continue;
-        const float v = topk_score(logits_row, bias, e);
-        if (topk_better(v, e, bs, bi)) {
-          bs = v;
-          bi = e;
-        }
+  }
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      if (key[s] > bk) {
+        bk = key[s];
+        bi = lane + 32 * s;
       }
-      // ... then the warp's: the largest score, and among its holders the
-      // lowest id (the same order as topk_better)
-      const uint32_t key = bi == 0x7fffffff ? 0u : score_key(bs);
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const int win = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
-      const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
-      if ((win & 31) == lane) taken |= 1u << (win >> 5);
-      sel[j] = ws;
-      ids[j] = win;
+    }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const int win = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)bi : 0xffffffffu);
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+      if (lane + 32 * s == win) key[s] = 0u;
+    const float ws = kmax ? key_score(kmax) : -CUDART_INF_F;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (jj == j) {
+        ids[jj] = win;
+        sel[jj] = ws;
+      }
     }
   }
   float total = 0.0f;
@@ -152,6 +168,12 @@ MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int 
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = j < k ? __fdiv_rn(sel[j], total) : 0.0f;
+}
+
+MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
+  if (E <= 64) topk_warp_s<2>(logits_row, bias, E, k, ids, w);
+  else if (E <= 256) topk_warp_s<8>(logits_row, bias, E, k, ids, w);
+  else topk_warp_s<32>(logits_row, bias, E, k, ids, w);
 }
 
 // ------------------------------------------------------------------ Q8
