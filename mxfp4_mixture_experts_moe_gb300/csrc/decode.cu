@@ -30,6 +30,7 @@ namespace {
 constexpr int kWarps = 29;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCons = kWarps - 1;  // warps 0..27 consume (<= 64 registers each); warp 28 produces
+constexpr int kGroup = kCons / 2;  // consumer warps per ring item (two items in flight)
 constexpr int kMaxA = 64;          // assignments T*k handled by the fused path
 
 struct DecodeArgs {
@@ -73,7 +74,6 @@ struct Misc {  // views into the small shared-memory region (A = T*k <= 64)
   int *segb;    // [A+1] start of the j-th expert segment (segb[nact] = A)
   int *active;  // [A] expert of the j-th segment, increasing id
   int *scalars; // [0] number of segments, [1] barrier flag
-  float *gu;    // [2][T][Rg][2] gate/up sums of the expert in flight (double buffer)
 };
 
 MOE_DEVFN Misc misc_view(uint8_t *base, int A) {
@@ -85,8 +85,7 @@ MOE_DEVFN Misc misc_view(uint8_t *base, int A) {
   m.skey = p; p += A;
   m.segb = p; p += A + 1;
   m.active = p; p += A;
-  m.scalars = p; p += 4;
-  m.gu = reinterpret_cast<float *>(p);
+  m.scalars = p;
   return m;
 }
 
@@ -308,12 +307,16 @@ MOE_DEVFN void rank_sort(const Misc &m, int A, int E, unsigned *status) {
   __syncthreads();
 }
 
-template <int SG, int SD>
+// SG, SD: 32-block groups per lane for the gate/up (K = H) and down (K = I)
+// rows.  FULL: H = 1024 SG and I = 1024 SD exactly, so every size below is a
+// compile-time constant.
+template <int SG, int SD, bool FULL>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int H = p.H, I = p.I, E = p.E, k = p.k, T = p.T, A = p.A;
+  const int H = FULL ? 1024 * SG : p.H, I = FULL ? 1024 * SD : p.I;
+  const int E = p.E, k = p.k, T = p.T, A = p.A;
   const int nbH = H / 32, nbI = I / 32;
   const int nstage = p.nstage;
 
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
-      mbar_init(smem_addr(&empty[s]), kCons);
+      mbar_init(smem_addr(&empty[s]), kGroup);
     }
     mbar_init(smem_addr(fbar), 1);
     fence_mbar_init();
@@ -474,31 +477,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   }
 
   // -------------------------------------------------------------- consumers
+  // Two groups of kGroup warps take alternate ring items (group g: items g,
+  // g+2, ...), so two items are computed at once.  A gate/up unit is one
+  // output row of the expert, both matrices in one warp, SwiGLU in the warp.
+  // A down unit is two rows of the down matrix sharing the activation loads.
+  // Before its first down item (or at the end, if it has none) every consumer
+  // warp joins the grid barrier, then all quantise h together.
   // A warp whose wait gave up stops computing but keeps arriving on the ring
   // and on the named barriers, so no other warp is left waiting on it.
-  bool dead = false;
-  for (int it = 0; it < 2 * nact; ++it) {
-    if (it == nact) {
-      // every CTA's h slice is written: quantise all A rows of h here
-      if (!grid_barrier(p.bar, base + 2ull * G, 2, kCons * 32, &m.scalars[1], p.status)) return;
-      for (int base = warp * 32; base < 2 * A * nbI; base += kCons * 32) {
-        const int idx = base + lane;  // 2 * block + half
-        const bool valid = idx < 2 * A * nbI;
-        const int blk = valid ? idx >> 1 : 0, half = idx & 1;
-        const int a = blk / nbI, b = blk - a * nbI;
-        float v[16];
-        const float *src = p.h + (int64_t)a * p.ld_h + 32 * b + 16 * half;
+  const int grp = warp / kGroup, gw = warp - grp * kGroup;
+  bool dead = false, h_ready = false;
+  auto quantise_h = [&]() -> bool {
+    // every CTA's h slice is written: quantise all A rows of h here
+    if (!grid_barrier(p.bar, base + 2ull * G, 2, kCons * 32, &m.scalars[1], p.status)) return false;
+    for (int base2 = warp * 32; base2 < 2 * A * nbI; base2 += kCons * 32) {
+      const int idx = base2 + lane;  // 2 * block + half
+      const bool valid = idx < 2 * A * nbI;
+      const int blk = valid ? idx >> 1 : 0, half = idx & 1;
+      const int a = blk / nbI, b = blk - a * nbI;
+      float v[16];
+      const float *src = p.h + (int64_t)a * p.ld_h + 32 * b + 16 * half;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
-          v[4 * c] = __uint_as_float(r.x);
-          v[4 * c + 1] = __uint_as_float(r.y);
-          v[4 * c + 2] = __uint_as_float(r.z);
-          v[4 * c + 3] = __uint_as_float(r.w);
-        }
-        q8_pair_to_row(v, half, valid, act + (uint32_t)a * p.hrow, I, b);
+      for (int c = 0; c < 4; ++c) {
+        const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
+        v[4 * c] = __uint_as_float(r.x);
+        v[4 * c + 1] = __uint_as_float(r.y);
+        v[4 * c + 2] = __uint_as_float(r.z);
+        v[4 * c + 3] = __uint_as_float(r.w);
       }
-      bar_sync_named(1, kCons * 32);
+      q8_pair_to_row(v, half, valid, act + (uint32_t)a * p.hrow, I, b);
+    }
+    bar_sync_named(1, kCons * 32);
+    return true;
+  };
+  for (int it = grp; it < 2 * nact; it += 2) {
+    if (it >= nact && !h_ready) {
+      if (!quantise_h()) return;
+      h_ready = true;
     }
     const int st = it % nstage;
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
@@ -506,46 +521,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     if (dead) {
       // skip the work
     } else if (it < nact) {
-      // units (output row r, matrix mm): gate and up of a row are summed by
-      // two warps and meet in shared memory for SwiGLU
       const int sb = m.segb[it], se = m.segb[it + 1];
-      float *gu = m.gu + (it & 1) * (T * p.Rg * 2);
-      for (int u = warp; u < 2 * Rg; u += kCons) {
-        const int r = u >> 1, mm = u & 1;
-        uint4 wq[1][SG];
-        float ws[1][SG];
-        load_weights_packed<1, SG>(sbase + mm * p.gwreg, 0, sbase + 2 * p.gwreg + mm * p.gsreg, 0, r, H, wq, ws);
+#pragma unroll 1
+      for (int r = gw; r < Rg; r += kGroup) {
+        const uint32_t wrow[2] = {sbase + (uint32_t)r * (H / 2), sbase + p.gwreg + (uint32_t)r * (H / 2)};
+        const uint32_t srow[2] = {sbase + 2 * p.gwreg + (uint32_t)r * nbH,
+                                  sbase + 2 * p.gwreg + p.gsreg + (uint32_t)r * nbH};
 #pragma unroll 1
         for (int q = sb; q < se; ++q) {
-          const int t = (int)__umulhi((unsigned)m.srt[q], p.kdiv);
-          float acc[1];
-          row_dot_smem_pn<1, SG>(act + (uint32_t)t * p.xrow, H, wq, ws, acc);
-          const float v = reduce_one(acc[0]);
-          if (lane == 0) gu[((q - sb) * p.Rg + r) * 2 + mm] = v;
+          const int a = m.srt[q];
+          const int t = (int)__umulhi((unsigned)a, p.kdiv);
+          float acc[2];
+          row_dot_stage_pn<2, SG>(act + (uint32_t)t * p.xrow, H, wrow, srow, acc);
+          float g, u;
+          reduce_pair(acc[0], acc[1], g, u);
+          if (lane == 0) p.h[(int64_t)a * p.ld_h + n0g + r] = __fmul_rn(silu(g), u);
         }
-      }
-      bar_sync_named(1, kCons * 32);
-      for (int idx = tid; idx < (se - sb) * Rg; idx += kCons * 32) {
-        const int ql = idx / Rg, r = idx - ql * Rg;
-        const float g = gu[(ql * p.Rg + r) * 2], u = gu[(ql * p.Rg + r) * 2 + 1];
-        p.h[(int64_t)m.srt[sb + ql] * p.ld_h + n0g + r] = __fmul_rn(silu(g), u);
       }
     } else {
       const int j = it - nact;
       const int sb = m.segb[j], se = m.segb[j + 1];
-      for (int r = warp; r < Rd; r += kCons) {
-        uint4 wq[1][SD];
-        float ws[1][SD];
-        load_weights_packed<1, SD>(sbase, p.dwreg, sbase + p.dwreg, 0, r, I, wq, ws);
+#pragma unroll 1
+      for (int r = gw; r < Rd; r += 2 * kGroup) {
+        const bool two = r + kGroup < Rd;
+        const int r2 = two ? r + kGroup : r;  // one row left: both halves read row r
+        const uint32_t wrow[2] = {sbase + (uint32_t)r * (I / 2), sbase + (uint32_t)r2 * (I / 2)};
+        const uint32_t srow[2] = {sbase + p.dwreg + (uint32_t)r * nbI, sbase + p.dwreg + (uint32_t)r2 * nbI};
 #pragma unroll 1
         for (int q = sb; q < se; ++q) {
           const int a = m.srt[q];
-          float acc[1];
-          row_dot_smem_pn<1, SD>(act + (uint32_t)a * p.hrow, I, wq, ws, acc);
-          const float v = reduce_one(acc[0]);
+          float acc[2];
+          row_dot_stage_pn<2, SD>(act + (uint32_t)a * p.hrow, I, wrow, srow, acc);
+          float v0, v1;
+          reduce_pair(acc[0], acc[1], v0, v1);
           if (lane == 0) {
-            yslice[a * p.Rd + r] = v;
-            if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v;
+            yslice[a * p.Rd + r] = v0;
+            if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v0;
+            if (two) {
+              yslice[a * p.Rd + r + kGroup] = v1;
+              if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r + kGroup] = v1;
+            }
           }
         }
       }
@@ -553,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
+  if (nact > 0 && !h_ready && !quantise_h()) return;
   bar_sync_named(1, kCons * 32);
   // combine of this CTA's output slice, slot order
   for (int idx = tid; idx < T * Rd; idx += kCons * 32) {
@@ -566,16 +582,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
 
 using DecodeKernel = void (*)(DecodeArgs);
 
-DecodeKernel pick(int sg, int sd) {
-  if (sg == 1 && sd == 1) return decode_kernel<1, 1>;
-  if (sg == 2 && sd == 1) return decode_kernel<2, 1>;
-  if (sg == 2 && sd == 2) return decode_kernel<2, 2>;
-  if (sg == 4 && sd == 2) return decode_kernel<4, 2>;
-  if (sg == 4 && sd == 4) return decode_kernel<4, 4>;
-  if (sg == 1 && sd == 2) return decode_kernel<1, 2>;
-  if (sg == 2 && sd == 4) return decode_kernel<2, 4>;
-  if (sg == 4 && sd == 1) return decode_kernel<4, 1>;
-  if (sg == 1 && sd == 4) return decode_kernel<1, 4>;
+DecodeKernel pick(int sg, int sd, bool full) {
+  if (full) {
+    if (sg == 4 && sd == 2) return decode_kernel<4, 2, true>;
+    if (sg == 4 && sd == 4) return decode_kernel<4, 4, true>;
+    if (sg == 2 && sd == 4) return decode_kernel<2, 4, true>;
+    if (sg == 2 && sd == 2) return decode_kernel<2, 2, true>;
+  }
+  if (sg == 1 && sd == 1) return decode_kernel<1, 1, false>;
+  if (sg == 2 && sd == 1) return decode_kernel<2, 1, false>;
+  if (sg == 2 && sd == 2) return decode_kernel<2, 2, false>;
+  if (sg == 4 && sd == 2) return decode_kernel<4, 2, false>;
+  if (sg == 4 && sd == 4) return decode_kernel<4, 4, false>;
+  if (sg == 1 && sd == 2) return decode_kernel<1, 2, false>;
+  if (sg == 2 && sd == 4) return decode_kernel<2, 4, false>;
+  if (sg == 4 && sd == 1) return decode_kernel<4, 1, false>;
+  if (sg == 1 && sd == 4) return decode_kernel<1, 4, false>;
   return nullptr;
 }
 
@@ -599,7 +621,7 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t act_bytes = align16(std::max<uint64_t>((uint64_t)T * p.xrow, (uint64_t)A * p.hrow));
   const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
-  const uint64_t misc_bytes = align16(4ull * (7 * A + 5) + 4ull * 2 * T * Rg * 2);
+  const uint64_t misc_bytes = align16(4ull * (7 * A + 5));
   const uint64_t tail = 16ull * 8 + act_bytes + y_bytes + logit_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   if (tail >= budget) return false;
@@ -684,7 +706,8 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   const int nbH = H / 32, nbI = I / 32;
   const int SG = (nbH + 31) / 32, SD = (nbI + 31) / 32;
   const int SGp = SG == 3 ? 4 : SG, SDp = SD == 3 ? 4 : SD;
-  DecodeKernel kern = pick(SGp, SDp);
+  const bool full = H == 1024 * SGp && I == 1024 * SDp;
+  DecodeKernel kern = pick(SGp, SDp, full);
   if (!kern) return fail(MOE_ERR_UNSUPPORTED, "%s: shape", name);
 
   DecodeArgs p{};
@@ -704,8 +727,8 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   p.g16 = nbH % 16 == 0 && (uintptr_t)sg % 16 == 0 && (uintptr_t)su % 16 == 0;
   p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0;
 
-  static bool configured[16][64] = {};
-  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2);
+  static bool configured[18][64] = {};
+  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2) + (full ? 9 : 0);
   if (dev < 64 && !configured[ki][dev]) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
     if (err != cudaSuccess) return cuda_fail(err, name);

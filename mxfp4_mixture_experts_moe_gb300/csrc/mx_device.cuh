@@ -408,6 +408,46 @@ MOE_DEVFN void row_dot_global(const int8_t *xr, const float *sr, int K, const ui
   }
 }
 
+// NM weight rows read block by block from shared memory (not preloaded into
+// registers) against one staged activation row: the form for weights that
+// are used by one activation row only.  wrow[m] / srow[m]: shared addresses of
+// row m's packed codes and scale bytes.  Same terms, same order per lane as
+// row_dot_smem_pn.
+template <int NM, int S>
+MOE_DEVFN void row_dot_stage_pn(uint32_t xrow, int K, const uint32_t (&wrow)[NM], const uint32_t (&srow)[NM],
+                                float (&acc)[NM]) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 32;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int b = lane + 32 * s;
+    if (b < nb) {
+      const uint4 lo = lds128(xrow + 16u * b), hi = lds128(xrow + 16u * (nb + b));
+      const float sx = lds_f32(xrow + (uint32_t)K + 4u * b);
+      const uint32_t xw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        const uint4 w = lds128(wrow[m] + 16u * b);
+        const float ws = e8m0_half(lds_u8(srow[m] + b));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        int dp = 0, dn = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t pl, ph, nl, nh;
+          e2m1x8_pos_neg(wv[j], pl, ph, nl, nh);
+          dp = __dp4a((int)xw[2 * j], (int)pl, dp);
+          dp = __dp4a((int)xw[2 * j + 1], (int)ph, dp);
+          dn = __dp4a((int)xw[2 * j], (int)nl, dn);
+          dn = __dp4a((int)xw[2 * j + 1], (int)nh, dn);
+        }
+        acc[m] = __fmaf_rn(__int2float_rn(dp - dn), __fmul_rn(sx, ws), acc[m]);
+      }
+    }
+  }
+}
+
 // Butterfly of two per-lane sums at once: lanes 0-15 finish the first, 16-31
 // the second, each with exactly the pairs and association of its own full
 // xor butterfly (so the bits equal two separate butterflies).  Lane 0 returns
