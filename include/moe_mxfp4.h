@@ -206,7 +206,8 @@ MOE_API moe_status moe_combine(const float *y, int64_t ld_y, const float *w, int
 
 /* ---------------------------------------------------------------- fused decode */
 
-/* Bytes of the workspace moe_decode_forward needs (grid-barrier counters). */
+/* Bytes of the workspace moe_decode_forward needs (a grid-barrier counter
+ * and one readiness counter per active expert). */
 MOE_API size_t moe_decode_workspace_bytes(void);
 
 /* Largest T that moe_decode_forward accepts for this layer shape on the

@@ -32,6 +32,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kCons = kWarps - 1;  // warps 0..27 consume (<= 64 registers each); warp 28 produces
 constexpr int kGroup = kCons / 2;  // consumer warps per ring item (two items in flight)
 constexpr int kMaxA = 64;          // assignments T*k handled by the fused path
+constexpr int kSlotWord = 8;       // first per-expert readiness word of the workspace
 
 struct DecodeArgs {
   const void *x;
@@ -52,7 +53,7 @@ struct DecodeArgs {
   int64_t ld_h;
   float *y;  // optional
   int64_t ld_y;
-  unsigned long long *bar;  // [0] arrival counter, [1] hold (0)
+  unsigned long long *bar;  // [0] arrival counter, [1] hold (0), [kSlotWord + j] h of expert slot j done
   unsigned *status;
   // geometry (host-computed)
   int nstage;
@@ -60,7 +61,7 @@ struct DecodeArgs {
   uint32_t gwreg, gsreg;  // gate/up stage: weight / scale region per matrix
   uint32_t dwreg;         // down stage: weight region
   uint32_t xrow, hrow;    // staged activation row bytes
-  uint32_t off_bars, off_act, off_y, off_logit, off_misc;
+  uint32_t off_bars, off_act, off_hbuf, off_y, off_logit, off_misc;
   int Rd;                 // max down rows per CTA (row stride of the y slice)
   int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
   int g16, d16;           // scale bytes copyable in 16-byte pieces
@@ -73,7 +74,7 @@ struct Misc {  // views into the small shared-memory region (A = T*k <= 64)
   int *skey;    // [A] expert at sorted position p
   int *segb;    // [A+1] start of the j-th expert segment (segb[nact] = A)
   int *active;  // [A] expert of the j-th segment, increasing id
-  int *scalars; // [0] number of segments, [1] barrier flag
+  int *scalars; // [0] number of segments, [1] barrier flag, [2 + g] wait result of group g
 };
 
 MOE_DEVFN Misc misc_view(uint8_t *base, int A) {
@@ -128,6 +129,22 @@ MOE_DEVFN bool grid_barrier(unsigned long long *ctr, unsigned long long target, 
   }
   bar_sync_named(bar_id, nthreads);
   return *reinterpret_cast<volatile int *>(flag) != 0;
+}
+
+// Wait (one thread) until *ctr >= target: acquire loads for at most
+// kBarrierTimeoutNs.  Returns false on timeout.
+MOE_DEVFN bool wait_count(unsigned long long *ctr, unsigned long long target, unsigned *status) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (i > (1u << 26) || globaltimer_ns() - t0 > kBarrierTimeoutNs) {
+      if (status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+    if (i >= 8) __nanosleep(32);
+  }
 }
 
 // 8 consecutive bf16 / fp32 values from shared memory, widened exactly.
@@ -388,6 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       q8_to_row(v, act + (uint32_t)t * p.xrow, H, b);
     }
   }
+  // CTA 0 clears the per-expert readiness words; barrier 1 publishes that
+  // before any CTA can count on them
+  if (cta == 0 && tid < kMaxA) p.bar[kSlotWord + tid] = 0ull;
   if (!grid_barrier(p.bar, base + (unsigned long long)G, 0, kThreads, &m.scalars[1], p.status)) return;
 
   // ---------------------------------------------------------------- A'
@@ -479,48 +499,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // -------------------------------------------------------------- consumers
   // Two groups of kGroup warps take alternate ring items (group g: items g,
   // g+2, ...), so two items are computed at once.  A gate/up unit is one
-  // output row of the expert, both matrices in one warp, SwiGLU in the warp.
-  // A down unit is two rows of the down matrix sharing the activation loads.
-  // Before its first down item (or at the end, if it has none) every consumer
-  // warp joins the grid barrier, then all quantise h together.
+  // output row of the expert, both matrices in one warp, SwiGLU in the warp;
+  // when a group has written its h slice of expert slot j it counts that in
+  // the workspace word of slot j.  A down item for slot j waits until all
+  // CTAs have counted, quantises that expert's h rows into the group's own
+  // buffer, then computes units of two down rows sharing the activation loads.
   // A warp whose wait gave up stops computing but keeps arriving on the ring
   // and on the named barriers, so no other warp is left waiting on it.
   const int grp = warp / kGroup, gw = warp - grp * kGroup;
-  bool dead = false, h_ready = false;
-  auto quantise_h = [&]() -> bool {
-    // every CTA's h slice is written: quantise all A rows of h here
-    if (!grid_barrier(p.bar, base + 2ull * G, 2, kCons * 32, &m.scalars[1], p.status)) return false;
-    for (int base2 = warp * 32; base2 < 2 * A * nbI; base2 += kCons * 32) {
-      const int idx = base2 + lane;  // 2 * block + half
-      const bool valid = idx < 2 * A * nbI;
-      const int blk = valid ? idx >> 1 : 0, half = idx & 1;
-      const int a = blk / nbI, b = blk - a * nbI;
-      float v[16];
-      const float *src = p.h + (int64_t)a * p.ld_h + 32 * b + 16 * half;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
-        v[4 * c] = __uint_as_float(r.x);
-        v[4 * c + 1] = __uint_as_float(r.y);
-        v[4 * c + 2] = __uint_as_float(r.z);
-        v[4 * c + 3] = __uint_as_float(r.w);
-      }
-      q8_pair_to_row(v, half, valid, act + (uint32_t)a * p.hrow, I, b);
-    }
-    bar_sync_named(1, kCons * 32);
-    return true;
-  };
+  const int gbar = 3 + grp;  // named barrier of this group
+  const uint32_t hbuf = smem_addr(smem + p.off_hbuf) + (uint32_t)grp * (uint32_t)T * p.hrow;
+  bool dead = false;
   for (int it = grp; it < 2 * nact; it += 2) {
-    if (it >= nact && !h_ready) {
-      if (!quantise_h()) return;
-      h_ready = true;
-    }
     const int st = it % nstage;
+    const int j = it - nact;  // expert slot of a down item
+    if (j >= 0) {
+      if (gw == 0 && lane == 0)
+        m.scalars[2 + grp] = !dead && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
+      bar_sync_named(gbar, kGroup * 32);
+      dead = dead || m.scalars[2 + grp] == 0;
+      if (!dead) {
+        const int sb = m.segb[j], nrow = m.segb[j + 1] - sb;
+        for (int idx0 = gw * 32; idx0 < 2 * nrow * nbI; idx0 += kGroup * 32) {
+          const int idx = idx0 + lane;  // 2 * block + half
+          const bool valid = idx < 2 * nrow * nbI;
+          const int blk = valid ? idx >> 1 : 0, half = idx & 1;
+          const int ql = blk / nbI, b = blk - ql * nbI;
+          float v[16];
+          const float *src = p.h + (int64_t)m.srt[sb + ql] * p.ld_h + 32 * b + 16 * half;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
+            v[4 * c] = __uint_as_float(r.x);
+            v[4 * c + 1] = __uint_as_float(r.y);
+            v[4 * c + 2] = __uint_as_float(r.z);
+            v[4 * c + 3] = __uint_as_float(r.w);
+          }
+          q8_pair_to_row(v, half, valid, hbuf + (uint32_t)ql * p.hrow, I, b);
+        }
+      }
+      bar_sync_named(gbar, kGroup * 32);
+    }
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
     if (dead) {
       // skip the work
-    } else if (it < nact) {
+    } else if (j < 0) {
       const int sb = m.segb[it], se = m.segb[it + 1];
 #pragma unroll 1
       for (int r = gw; r < Rg; r += kGroup) {
@@ -539,7 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         }
       }
     } else {
-      const int j = it - nact;
       const int sb = m.segb[j], se = m.segb[j + 1];
 #pragma unroll 1
       for (int r = gw; r < Rd; r += 2 * kGroup) {
@@ -551,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         for (int q = sb; q < se; ++q) {
           const int a = m.srt[q];
           float acc[2];
-          row_dot_stage_pn<2, SD>(act + (uint32_t)a * p.hrow, I, wrow, srow, acc);
+          row_dot_stage_pn<2, SD>(hbuf + (uint32_t)(q - sb) * p.hrow, I, wrow, srow, acc);
           float v0, v1;
           reduce_pair(acc[0], acc[1], v0, v1);
           if (lane == 0) {
@@ -565,10 +588,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         }
       }
     }
+    if (j < 0) {
+      // this CTA's h slice of expert slot it is written: count it (release)
+      bar_sync_named(gbar, kGroup * 32);
+      if (gw == 0 && lane == 0)
+        asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSlotWord + it), "l"(1ull) : "memory");
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
-  if (nact > 0 && !h_ready && !quantise_h()) return;
   bar_sync_named(1, kCons * 32);
   // combine of this CTA's output slice, slot order
   for (int idx = tid; idx < T * Rd; idx += kCons * 32) {
@@ -618,11 +646,12 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.stage_bytes = ((gstage > dstage ? gstage : dstage) + 127u) & ~127u;
   p.xrow = (uint32_t)H + 8u * nbH;
   p.hrow = (uint32_t)I + 8u * nbI;
-  const uint64_t act_bytes = align16(std::max<uint64_t>((uint64_t)T * p.xrow, (uint64_t)A * p.hrow));
+  const uint64_t act_bytes = align16((uint64_t)T * p.xrow);
+  const uint64_t hbuf_bytes = align16(2ull * T * p.hrow);  // one T-row buffer per consumer group
   const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
-  const uint64_t misc_bytes = align16(4ull * (7 * A + 5));
-  const uint64_t tail = 16ull * 8 + act_bytes + y_bytes + logit_bytes + misc_bytes;
+  const uint64_t misc_bytes = align16(4ull * (7 * A + 5));  // ids w srt skey segb active + 4 scalars
+  const uint64_t tail = 16ull * 8 + act_bytes + hbuf_bytes + y_bytes + logit_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   if (tail >= budget) return false;
   int ns = (int)((budget - tail) / p.stage_bytes);
@@ -635,7 +664,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   if (ring + tail > budget) return false;
   p.off_bars = (uint32_t)ring;
   p.off_act = p.off_bars + 16 * 8;
-  p.off_y = p.off_act + (uint32_t)act_bytes;
+  p.off_hbuf = p.off_act + (uint32_t)act_bytes;
+  p.off_y = p.off_hbuf + (uint32_t)hbuf_bytes;
   p.off_logit = p.off_y + (uint32_t)y_bytes;
   p.off_misc = p.off_logit + (uint32_t)logit_bytes;
   *smem_out = p.off_misc + misc_bytes;
@@ -647,7 +677,7 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
 
 using namespace moe;
 
-extern "C" size_t moe_decode_workspace_bytes(void) { return 64; }  // [0] counter, [1] hold, spare
+extern "C" size_t moe_decode_workspace_bytes(void) { return 8 * (kSlotWord + kMaxA); }
 
 extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) {
   if (H <= 0 || E <= 0 || k <= 0 || k > 8 || I <= 0 || H % 128 || I % 128 || H > 4096 || I > 4096 || E > 256) return 0;

@@ -28,14 +28,13 @@ namespace {
 constexpr int kScratchMaxSlots = 64;        // T * k
 constexpr int kScratchMaxLogits = 32768;    // T * E
 constexpr int kScratchMaxI = 4096;          // expert intermediate width
-constexpr size_t kOffBar = 0;               // 8 x u64 grid-barrier words
-constexpr size_t kOffIds = 256;             // int32 [T*k]
+constexpr size_t kBarBytes = 1024;          // grid-barrier and readiness words (>= moe_decode_workspace_bytes)
+constexpr size_t kOffBar = 0;
+constexpr size_t kOffIds = kBarBytes;       // int32 [T*k]
 constexpr size_t kOffW = kOffIds + 4 * kScratchMaxSlots;
-constexpr size_t kOffLogits = 1024;         // fp32 [T][E]
+constexpr size_t kOffLogits = kOffW + 4 * kScratchMaxSlots;  // fp32 [T][E]
 constexpr size_t kOffH = kOffLogits + 4 * (size_t)kScratchMaxLogits;  // fp32 [T*k][I]
 constexpr size_t kScratchBytes = kOffH + 4 * (size_t)kScratchMaxSlots * kScratchMaxI;
-constexpr size_t kBarBytes = 64;
-static_assert(kOffW + 4 * kScratchMaxSlots <= kOffLogits, "scratch layout");
 static_assert(kOffH % 256 == 0, "h rows must stay 16-byte aligned");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -79,11 +78,13 @@ extern "C" moe_status moe_decode_forward_noalloc(const void *x, moe_dtype x_dtyp
   if ((int64_t)T * E > kScratchMaxLogits)
     return fail(MOE_ERR_UNSUPPORTED, "%s: T*E=%lld exceeds the fixed scratch limit of %d", name, (long long)T * E, kScratchMaxLogits);
   if (I > kScratchMaxI) return fail(MOE_ERR_UNSUPPORTED, "%s: I=%d exceeds the fixed scratch limit of %d", name, I, kScratchMaxI);
+  if (moe_decode_workspace_bytes() > kBarBytes) return fail(MOE_ERR_UNSUPPORTED, "%s: workspace layout", name);
   unsigned char *s = nullptr;
   moe_status st = scratch_for_current_device(&s);
   if (st != MOE_OK) return st;
-  // The barrier counter and its hold word must start at zero; the
-  // other regions are written before they are read within one launch.
+  // The barrier counter and its hold word must start at zero (the kernel
+  // clears the readiness words itself); the other regions are written before
+  // they are read within one launch.
   cudaError_t err = cudaMemsetAsync(s + kOffBar, 0, kBarBytes, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "moe_decode_forward_noalloc: clearing the barrier words");
   return moe_decode_forward(x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd, T, H, E, k, I, out,
