@@ -327,6 +327,46 @@ MOE_DEVFN void rank_sort(const Misc &m, int A, int E, unsigned *status) {
 // SG, SD: 32-block groups per lane for the gate/up (K = H) and down (K = I)
 // rows.  FULL: H = 1024 SG and I = 1024 SD exactly, so every size below is a
 // compile-time constant.
+// rank_sort by one warp (the whole warp calls it) for A <= 32 assignments:
+// the same ranks, segments and flags, with the ranks counted over shuffled
+// ids and the segments cut with one ballot.
+MOE_DEVFN void rank_sort_warp(const Misc &m, int A, int E, unsigned *status) {
+  const int lane = threadIdx.x & 31;
+  int e = E;
+  if (lane < A) {
+    e = m.ids[lane];
+    if (e < 0 || e >= E) {
+      e = E;
+      if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    }
+  }
+  int rank = 0;
+#pragma unroll 1
+  for (int b = 0; b < A; ++b) {
+    const int eb = __shfl_sync(0xffffffffu, e, b);
+    rank += (eb < e) || (eb == e && b < lane);
+  }
+  if (lane < A) {
+    m.srt[rank] = lane;
+    m.skey[rank] = e;
+  }
+  __syncwarp();
+  const int kq = lane < A ? m.skey[lane] : E;
+  const int kp = (lane > 0 && lane < A) ? m.skey[lane - 1] : -1;
+  const bool st = lane < A && kq < E && (lane == 0 || kq != kp);
+  const unsigned bal = __ballot_sync(0xffffffffu, st);
+  if (st) {
+    const int j = __popc(bal & ((1u << lane) - 1u));
+    m.segb[j] = lane;
+    m.active[j] = kq;
+  }
+  const int nvalid = __popc(__ballot_sync(0xffffffffu, lane < A && kq < E));
+  if (lane == 0) {
+    m.segb[__popc(bal)] = nvalid;
+    m.scalars[0] = __popc(bal);
+  }
+}
+
 template <int SG, int SD, bool FULL>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -416,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   if (warp < T) {
     int id[8];
     float wv[8];
-    topk_warp_s<8>(logit_s + warp * E, p.bias, E, k, id, wv);  // E <= 256 on this path
+    topk_warp_sorted<8>(logit_s + warp * E, p.bias, E, k, id, wv);  // E <= 256 on this path
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k && lane == j) {
@@ -429,11 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       }
     }
   }
-  __syncthreads();
-  rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
+  if (T > 1) __syncthreads();  // one token: warp 0 wrote every id itself
+  else __syncwarp();
+  if (A <= 32) {
+    if (warp == 0) rank_sort_warp(m, A, E, cta == 0 ? p.status : nullptr);
+    __syncthreads();
+  } else {
+    rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
+  }
   const int nact = m.scalars[0];
-  const int n0g = (int)((int64_t)cta * I / G), Rg = (int)((int64_t)(cta + 1) * I / G) - n0g;
-  const int n0d = (int)((int64_t)cta * H / G), Rd = (int)((int64_t)(cta + 1) * H / G) - n0d;
+  // this CTA's output slices (G * 4096 fits 32 bits)
+  const int n0g = (int)((unsigned)(cta * I) / (unsigned)G), Rg = (int)((unsigned)((cta + 1) * I) / (unsigned)G) - n0g;
+  const int n0d = (int)((unsigned)(cta * H) / (unsigned)G), Rd = (int)((unsigned)((cta + 1) * H) / (unsigned)G) - n0d;
 
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
@@ -449,33 +496,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       if (it < nact) {
         const int64_t row0 = (int64_t)m.active[it] * I + n0g;
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, 2 * gw);
+          mbar_arrive_expect_tx(fb, 2 * gw + (p.g16 ? 2 * gs : 0u));
           if (gw > 0) {  // a CTA may own no gate/up rows when I < #SMs
             bulk_g2s(sbase, p.wg + row0 * (H / 2), gw, fb, pol);
             bulk_g2s(sbase + p.gwreg, p.wu + row0 * (H / 2), gw, fb, pol);
+            if (p.g16) {  // the slice's scale bytes are one contiguous 16-byte-aligned run
+              bulk_g2s(sbase + 2 * p.gwreg, p.sg + row0 * nbH, gs, fb, pol);
+              bulk_g2s(sbase + 2 * p.gwreg + p.gsreg, p.su + row0 * nbH, gs, fb, pol);
+            }
           }
         }
+        if (!p.g16) {
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-          const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
-          const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
-          if (p.g16) {
-            for (uint32_t c = lane; c < gs / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
-          } else {
+          for (int mm = 0; mm < 2; ++mm) {
+            const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
+            const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
             for (uint32_t c = lane; c < gs / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
           }
         }
       } else {
         const int64_t row0 = (int64_t)m.active[it - nact] * H + n0d;
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, dw);
-          if (dw > 0) bulk_g2s(sbase, p.wd + row0 * (I / 2), dw, fb, pol);
+          mbar_arrive_expect_tx(fb, dw + (p.d16 ? ds : 0u));
+          if (dw > 0) {
+            bulk_g2s(sbase, p.wd + row0 * (I / 2), dw, fb, pol);
+            if (p.d16) bulk_g2s(sbase + p.dwreg, p.sd + row0 * nbI, ds, fb, pol);
+          }
         }
-        const uint8_t *src = p.sd + row0 * nbI;
-        const uint32_t dst = sbase + p.dwreg;
-        if (p.d16) {
-          for (uint32_t c = lane; c < ds / 16; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
-        } else {
+        if (!p.d16) {
+          const uint8_t *src = p.sd + row0 * nbI;
+          const uint32_t dst = sbase + p.dwreg;
           for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
         }
       }

@@ -117,9 +117,9 @@ MOE_DEVFN float key_score(uint32_t key) {  // inverse of score_key on real score
 // S = scores per lane (expert lane + 32 s); E <= 32 * S.  Each lane reads its
 // scores once, then every round is register work: the lane's best key (the
 // first of equal keys has the lower id), the warp's largest key, and the
-// lowest id holding it.
+// lowest id holding it.  Used for large S.
 template <int S>
-MOE_DEVFN void topk_warp_s(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
+MOE_DEVFN void topk_warp_scan(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
   const int lane = threadIdx.x & 31;
   uint32_t key[S];
 #pragma unroll
@@ -170,10 +170,74 @@ MOE_DEVFN void topk_warp_s(const float *logits_row, const float *bias, int E, in
   for (int j = 0; j < 8; ++j) w[j] = j < k ? __fdiv_rn(sel[j], total) : 0.0f;
 }
 
+// The same selection for small S: each lane first sorts its S entries by
+// (key desc, id asc) with a stable odd-even transposition sort, so a round
+// only reads the lane's head entry, and the winning lane pops it.  Slot j's
+// id and score stay in lane j; the weights are formed there (the sum over
+// the slots is taken in slot order, as in topk_warp_scan) and broadcast.
+template <int S>
+MOE_DEVFN void topk_warp_sorted(const float *logits_row, const float *bias, int E, int k, int (&ids)[8],
+                                float (&w)[8]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[S];
+  int kid[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int e = lane + 32 * s;
+    key[s] = e < E ? score_key(topk_score(logits_row, bias, e)) : 0u;
+    kid[s] = e;
+  }
+#pragma unroll
+  for (int pass = 0; pass < S; ++pass) {
+#pragma unroll
+    for (int s = pass & 1; s + 1 < S; s += 2) {
+      if (key[s + 1] > key[s]) {  // strict: equal keys keep their id order
+        const uint32_t tk = key[s];
+        key[s] = key[s + 1];
+        key[s + 1] = tk;
+        const int ti = kid[s];
+        kid[s] = kid[s + 1];
+        kid[s + 1] = ti;
+      }
+    }
+  }
+  int my_id = 0;
+  float my_sel = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const uint32_t bk = key[0];
+    const int bi = bk ? kid[0] : 0x7fffffff;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const int win = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)bi : 0xffffffffu);
+    if (bk == kmax && bi == win) {
+#pragma unroll
+      for (int s = 0; s + 1 < S; ++s) {
+        key[s] = key[s + 1];
+        kid[s] = kid[s + 1];
+      }
+      key[S - 1] = 0u;
+    }
+    if (lane == j) {
+      my_id = win;
+      my_sel = kmax ? key_score(kmax) : -CUDART_INF_F;
+    }
+  }
+  const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-my_sel)));
+  float total = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) total = __fadd_rn(total, __shfl_sync(0xffffffffu, sg, j));
+  const float my_w = __fdiv_rn(sg, total);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ids[j] = j < k ? __shfl_sync(0xffffffffu, my_id, j) : 0;
+    w[j] = j < k ? __shfl_sync(0xffffffffu, my_w, j) : 0.0f;
+  }
+}
+
 MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
-  if (E <= 64) topk_warp_s<2>(logits_row, bias, E, k, ids, w);
-  else if (E <= 256) topk_warp_s<8>(logits_row, bias, E, k, ids, w);
-  else topk_warp_s<32>(logits_row, bias, E, k, ids, w);
+  if (E <= 64) topk_warp_sorted<2>(logits_row, bias, E, k, ids, w);
+  else if (E <= 256) topk_warp_sorted<8>(logits_row, bias, E, k, ids, w);
+  else topk_warp_scan<32>(logits_row, bias, E, k, ids, w);
 }
 
 // ------------------------------------------------------------------ Q8
