@@ -19,6 +19,22 @@ moe_status cuda_fail(cudaError_t e, const char *what);
 unsigned *device_status_word();  // per-device address of the status word, or NULL
 int sm_count();
 
+// Tensor-core path of the expert projections (tc_expert.cu): nm = 2 gate/up
+// with SwiGLU into out, nm = 1 down into out.  Used by the stage calls for
+// batches of more than kTensorMinRows - 1 rows.
+constexpr int kTensorMinRows = 17;
+moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
+                            const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
+                            const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
+                            int K, int N, int bytoken, float *out, int64_t ld_out, cudaStream_t stream,
+                            const char *name);
+
+// Token of assignment a = t*k + j, i.e. a / k, as a multiply-high by
+// kdiv_of(k) = ceil(2^32 / k), exact for a < 2^28 and k <= 8.  k = 1 is
+// encoded as 0 (ceil(2^32 / 1) does not fit 32 bits) and is the identity.
+inline uint32_t kdiv_of(int k) { return k <= 1 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k); }
+MOE_DEVFN int token_of(int a, uint32_t kdiv) { return kdiv ? (int)__umulhi((unsigned)a, kdiv) : a; }
+
 // ------------------------------------------------------------------ formats
 
 // E8M0 byte u -> 2^(u-128) as fp32 (the E8M0 factor 2^(u-127) halved, because

@@ -43,7 +43,7 @@ struct DecodeArgs {
   const float *bias;
   const uint8_t *wg, *sg, *wu, *su, *wd, *sd;
   int T, H, E, k, I, A;
-  uint32_t kdiv;  // ceil(2^32 / k)
+  uint32_t kdiv;  // kdiv_of(k): token of assignment a = token_of(a, kdiv)
   float *out;
   int64_t ld_out;
   float *logits;
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
 #pragma unroll 1
         for (int q = sb; q < se; ++q) {
           const int a = m.srt[q];
-          const int t = (int)__umulhi((unsigned)a, p.kdiv);
+          const int t = token_of(a, p.kdiv);
           float acc[2];
           row_dot_stage_pn<2, SG>(act + (uint32_t)t * p.xrow, H, wrow, srow, acc);
           float g, u;
@@ -795,7 +795,7 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   p.wr = w_router; p.wbf = w_dtype == MOE_BF16; p.bias = bias;
   p.wg = wg; p.sg = sg; p.wu = wu; p.su = su; p.wd = wd; p.sd = sd;
   p.T = T; p.H = H; p.E = E; p.k = k; p.I = I; p.A = A;
-  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
+  p.kdiv = kdiv_of(k);
   p.out = out; p.ld_out = ld_out; p.logits = logits; p.ids = ids; p.weights = weights;
   p.h = h; p.ld_h = ld_h; p.y = y; p.ld_y = ld_y;
   p.bar = static_cast<unsigned long long *>(workspace);

@@ -19,6 +19,11 @@ MOE_DEVFN float lds_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr));
   return r;
 }
+MOE_DEVFN uint32_t lds_u32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
 MOE_DEVFN int lds_s32(uint32_t addr) {
   int r;
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(r) : "r"(addr));

@@ -44,7 +44,7 @@ struct MxArgs {
   int K;  // reduction length
   int N;  // output rows per expert
   int n_act;          // activation rows: T (gate/up) or A (down)
-  uint32_t kdiv;      // ceil(2^32 / k): token of assignment a = umulhi(a, kdiv)
+  uint32_t kdiv;      // kdiv_of(k): token of assignment a = token_of(a, kdiv)
   float *out0, *out1;
   int64_t ld_out;
   int R;              // output rows per CTA (max)
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   if (p.rowtab) {
     for (int q = tid; q < nsorted; q += ncons * 32) {
       const int a = p.sorted[q];
-      rowtab[q] = a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : (int)__umulhi((unsigned)a, p.kdiv)));
+      rowtab[q] = a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : token_of(a, p.kdiv)));
     }
   }
   // Stage every activation row once: codes in two half-block planes, the
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
             if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
             continue;
           }
-          arow = MODE == kDown ? a : (int)__umulhi((unsigned)a, p.kdiv);
+          arow = MODE == kDown ? a : token_of(a, p.kdiv);
         }
         float acc[NM];
         if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
@@ -326,16 +326,19 @@ static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const f
   if (!wu) return fail(MOE_ERR_INVALID_ARG, "%s: null up weights", name);
   if (ld < I) return fail(MOE_ERR_INVALID_ARG, "%s: output ld=%lld < I=%d", name, (long long)ld, I);
   if (mode == kGateUpRaw && (!o1 || (uintptr_t)o1 % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: bad up output", name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mode == kGateUpSwiglu && T >= kTensorMinRows)
+    return launch_tc_expert(2, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T * k, k, E, H, I, 1, o0,
+                            ld, s, name);
   MxArgs p{};
   p.aq = xq; p.ld_aq = ld_xq; p.as = xs; p.ld_as = ld_xs;
   p.w0 = wg; p.s0 = sg; p.w1 = wu; p.s1 = su;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
   p.A = T * k; p.k = k; p.E = E; p.K = H; p.N = I;
   p.n_act = T;
-  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
+  p.kdiv = kdiv_of(k);
   p.out0 = o0; p.out1 = o1; p.ld_out = ld;
   p.status = device_status_word();
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   return mode == kGateUpSwiglu ? launch_mx<kGateUpSwiglu>(p, s, name) : launch_mx<kGateUpRaw>(p, s, name);
 }
 
@@ -365,13 +368,16 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
                                H, I, y, ld_y, I, T * k);
   if (st != MOE_OK || T == 0) return st;
   if (ld_y < H) return fail(MOE_ERR_INVALID_ARG, "%s: ld_y=%lld < H=%d", name, (long long)ld_y, H);
+  if (T >= kTensorMinRows)
+    return launch_tc_expert(1, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T * k, k, E, I,
+                            H, 0, y, ld_y, static_cast<cudaStream_t>(stream), name);
   MxArgs p{};
   p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
   p.w0 = wd; p.s0 = sd;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
   p.A = T * k; p.k = k; p.E = E; p.K = I; p.N = H;
   p.n_act = T * k;
-  p.kdiv = (uint32_t)((0x100000000ull + (uint64_t)k - 1) / (uint64_t)k);
+  p.kdiv = kdiv_of(k);
   p.out0 = y; p.ld_out = ld_y;
   p.status = device_status_word();
   return launch_mx<kDown>(p, static_cast<cudaStream_t>(stream), name);

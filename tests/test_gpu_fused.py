@@ -147,3 +147,20 @@ def test_fused_nan_scores_are_flagged_not_followed(moe, dsv4):
         ws = moe.Workspace(1, dsv4, "cuda")
         moe.MoeLayer(dsv4, fused=fused).forward(x, ws)
         assert moe.moe_device_status() & moe.MOE_DEV_BAD_EXPERT_ID
+
+
+def test_fused_single_expert_per_token(moe):
+    """k = 1 (one expert per token): the assignment is the token itself, in the
+    fused kernel and in the stage calls alike."""
+    spec = synth.LayerSpec(H=256, E=8, k=1, I=128, x_dtype="f32", wr_dtype="f32", seed=41)
+    lw = upload_layer(spec)
+    for T in (1, 4):
+        x = dev(synth.activations(spec, T, token0=50))
+        a, b = _forward(moe, lw, x, True), _forward(moe, lw, x, False)
+        _same(a, b)
+        xs = synth.activations(spec, T, token0=50)
+        _, ids, _ = oracle.route(xs, synth.router_weights(spec), spec.k)
+        r = oracle.layer(xs, synth.router_weights(spec), None, spec.k,
+                         {e: synth.expert(spec, e) for e in np.unique(ids).tolist()})
+        assert max_err_over_rms(host(a.out), r["out"]) <= TOL
+    assert moe.moe_device_status() == 0

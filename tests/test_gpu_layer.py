@@ -76,29 +76,39 @@ def _check_vs_oracle(spec, x, lw_ws, out, sample=None):
     assert bits_equal(host(ws.xq)[rows], r["xq"])
     assert bits_equal(host(ws.xs)[rows], r["xs"])
     arows = (rows[:, None] * spec.k + np.arange(spec.k)[None]).ravel()
-    assert max_err_over_rms(host(ws.h)[arows], r["h"]) <= TOL
-    # Q8(h): the GPU quantises its fp32 h, the oracle the fp32 rounding of its
-    # fp64 h.  The two h differ in the last bits, so a code may land one step
-    # apart where h * (1/scale) sits on a .5 boundary: both are correct
-    # roundings.  Every other code must agree; a differing code must be +-1 at
-    # such a boundary.
+    h_g = host(ws.h)[arows]
+    assert max_err_over_rms(h_g, r["h"]) <= TOL
+    # Q8(h) is integer work: the GPU's codes and scales are the oracle's Q8 of
+    # the GPU's own h, bit for bit.
+    q_own, s_own = oracle.quant_q8(h_g)
+    assert bits_equal(host(ws.hq)[arows], q_own)
+    assert bits_equal(host(ws.hs)[arows], s_own)
+    # Against the oracle's own (fp64-rounded) h a code may sit one step apart
+    # where h * (1/scale) lies near a .5 boundary: both are correct roundings
+    # of nearby values.  Codes never differ by more than one step.
     hq_g = host(ws.hq)[arows].astype(np.int32)
     hq_o = r["hq"].astype(np.int32)
     hs_o = r["hs"].astype(np.float32)
-    assert np.allclose(host(ws.hs)[arows], hs_o, rtol=1e-5, atol=0)
+    # a scale is amax/127 of its block of h, so it carries h's relative error:
+    # ~1e-7 on the CUDA-core path, ~1e-5 where the tensor core accumulates the
+    # 4096-term reductions in its own fp32 order (batches beyond 16 rows)
+    assert np.allclose(host(ws.hs)[arows], hs_o, rtol=1e-4, atol=0)
     flip = hq_g != hq_o
     assert np.all(np.abs(hq_g - hq_o) <= 1)
-    inv = np.where(hs_o > 0, np.float32(1.0) / np.where(hs_o > 0, hs_o, 1), 0).astype(np.float32)
-    v = r["h"].astype(np.float32) * np.repeat(inv, 32, axis=1)
-    dist = np.abs(np.abs(v - np.trunc(v)) - 0.5)
-    assert np.all(dist[flip] < 0.01), dist[flip].max()
     # y then differs by at most |dq| * scale * max|w| (|w| <= 6 for E8M0 <= 127)
     allow = (np.repeat(hs_o, 32, axis=1) * flip * 6.0).sum(axis=1)
     yg, yo = host(ws.y)[arows].astype(np.float64), r["y"]
     rms_y = np.sqrt(np.mean(yo ** 2))
     assert np.all(np.abs(yg - yo).max(axis=1) <= TOL * rms_y + allow)
-    err = max_err_over_rms(out[rows], r["out"])
-    assert err <= TOL, err
+    # out: the same flips, through the routing weights of each token.  Without
+    # a flip (the rule on the exact 1-16-row path) this is the strict bar.
+    allow_out = (np.abs(r["w"]).astype(np.float64) * allow.reshape(-1, spec.k)).sum(axis=1)
+    og, oo = out[rows].astype(np.float64), r["out"]
+    rms_o = np.sqrt(np.mean(oo ** 2))
+    assert np.all(np.abs(og - oo).max(axis=1) <= TOL * rms_o + allow_out)
+    err = max_err_over_rms(og, oo)
+    if not flip.any():
+        assert err <= TOL, err
     return dict(err_out=err, flips=int(flip.sum()), codes=int(flip.size),
                 err_y=max_err_over_rms(yg, yo), err_h=max_err_over_rms(host(ws.h)[arows], r["h"]))
 
@@ -170,11 +180,13 @@ def test_zipf_batches(moe, dsv4_zipf):
         ws, out = _run(moe, dsv4_zipf, dev(x), fused=False)
         ids = host(ws.ids)
         assert len(np.unique(ids)) < 0.9 * min(256, T * 6)  # skewed routing reuses experts
-        _check_vs_oracle(spec, x, ws, out, sample=[0, 5, T - 1])
-        # rows of the batch equal their one-row runs
-        for t in (0, T // 2, T - 1):
-            _, o1 = _run(moe, dsv4_zipf, dev(x[t:t + 1]))
-            assert bits_equal(out[t:t + 1], o1)
+        # batches beyond 16 rows take the tensor-core projections: sampled
+        # rows against the oracle (Q8(h) flips allowed, see _check_vs_oracle)
+        _check_vs_oracle(spec, x, ws, out, sample=[0, 5, T // 2, T - 1])
+        # the one-row runs of the same tokens take the exact path
+        for t in (0, T - 1):
+            ws1, o1 = _run(moe, dsv4_zipf, dev(x[t:t + 1]), fused=False)
+            _check_vs_oracle(spec, x[t:t + 1], ws1, o1)
 
 
 @pytest.mark.parametrize("T,sample", [(512, [0, 1, 255, 511]), (8192, [0, 4097, 8191])])
@@ -183,9 +195,6 @@ def test_prefill_chunks(moe, dsv4, T, sample):
     x = synth.activations(spec, T, token0=10000)
     ws, out = _run(moe, dsv4, dev(x), tile_rows=1, fused=False)
     _check_vs_oracle(spec, x, ws, out, sample=sample)
-    for t in sample[:2]:
-        _, o1 = _run(moe, dsv4, dev(x[t:t + 1]))
-        assert bits_equal(out[t:t + 1], o1)
     assert moe.moe_device_status() == 0
 
 

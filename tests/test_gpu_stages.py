@@ -152,7 +152,7 @@ def _stack(experts, E, name):
 
 @pytest.mark.parametrize("H,I,E,k,T,exact", [(4096, 256, 3, 2, 5, True), (256, 128, 8, 2, 3, True),
                                              (384, 640, 5, 3, 4, True), (4096, 256, 3, 2, 5, False),
-                                             (512, 384, 6, 6, 17, False)])
+                                             (512, 384, 6, 6, 17, False), (256, 128, 4, 1, 6, True)])
 def test_gateup(moe, H, I, E, k, T, exact):
     spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=21)
     ex = _experts(spec, E)
@@ -192,7 +192,8 @@ def test_gateup(moe, H, I, E, k, T, exact):
 
 
 @pytest.mark.parametrize("H,I,E,k,T,exact", [(4096, 2048, 3, 2, 3, True), (256, 128, 8, 2, 3, True),
-                                             (384, 640, 5, 3, 4, False), (4096, 2048, 2, 2, 4, False)])
+                                             (384, 640, 5, 3, 4, False), (4096, 2048, 2, 2, 4, False),
+                                             (256, 128, 4, 1, 5, True)])
 def test_down(moe, H, I, E, k, T, exact):
     spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=22)
     ex = _experts(spec, E)

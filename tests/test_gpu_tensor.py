@@ -1,0 +1,135 @@
+"""The tensor-core (tcgen05) expert projections, taken by the stage calls for
+batches of more than 16 rows, against the oracle.
+
+These GEMMs accumulate the whole reduction in fp32 on the tensor core with
+f16 operands: exact MXFP4 weights (E2M1 x a power of two per row) and the
+f16 rounding of the dequantised Q8 activations.  So the bar is the layer's
+floating-point tolerance, max|err| <= 1e-3 * RMS, not per-block bit
+identity (that bar, and the exact-rows contract, belong to 1-16 rows).
+Cases span several 128-row weight tiles, experts with more than 128 rows
+(several token tiles), experts with a handful of rows, padded segments and
+ragged reduction lengths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, dev, ensure_built, host, max_err_over_rms
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return ensure_built()
+
+
+def _skewed_rows(T, k, E, seed, hot):
+    """Top-k ids per token: expert `hot` in every row, the rest spread."""
+    ids = np.empty((T, k), np.int32)
+    for t in range(T):
+        r = synth.raw_u64(seed, 3000 + t, 0, E)
+        order = [e for e in np.argsort(r, kind="stable").tolist() if e != hot]
+        ids[t] = np.array([hot] + order[: k - 1], np.int32)
+    return ids
+
+
+def _stack(experts, E, name):
+    return torch.from_numpy(np.stack([getattr(experts[e], name) for e in range(E)])).cuda()
+
+
+@pytest.mark.parametrize("H,I,E,k,T,tile", [(4096, 256, 5, 2, 300, 1), (512, 384, 7, 3, 41, 4),
+                                            (256, 128, 3, 2, 17, 1)])
+def test_tensor_gateup_swiglu(moe, H, I, E, k, T, tile):
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=31)
+    ex = {e: synth.expert(spec, e) for e in range(E)}
+    xs = synth.positive_scales(31, 2101, T, H // 32)
+    xq = synth.int8_codes(31, 2100, T, H)
+    ids = _skewed_rows(T, k, E, 31, hot=E - 1)  # one expert takes every row: > 128 when T > 128
+    offsets, srt, _ = oracle.sort(ids, E, tile)
+    cap = moe.moe_sort_tokens_capacity(T, k, E, tile)
+    srt_full = np.concatenate([srt, np.full(cap - srt.size, -1, np.int32)])
+    W = {n: _stack(ex, E, n) for n in ("wg", "sg", "wu", "su")}
+    h = torch.full((T * k, I + 8), float("nan"), device="cuda")[:, :I]
+    moe.moe_mxfp4_gateup_swiglu(dev(xq, 16), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets),
+                                dev(srt_full), k, h)
+    ho = np.empty((T * k, I))
+    for a in range(T * k):
+        e = ex[ids.ravel()[a]]
+        g, u = oracle.expert_gateup(xq[a // k], xs[a // k], e.wg, e.sg, e.wu, e.su)
+        ho[a] = np.vectorize(oracle.silu)(g) * u
+    hg = host(h)
+    assert np.isfinite(hg).all()
+    assert max_err_over_rms(hg, ho) <= TOL
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("H,I,E,k,T,tile", [(4096, 2048, 3, 2, 150, 4), (384, 640, 6, 3, 20, 1)])
+def test_tensor_down(moe, H, I, E, k, T, tile):
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=32)
+    ex = {e: synth.expert(spec, e) for e in range(E)}
+    A = T * k
+    hs = synth.positive_scales(32, 2201, A, I // 32)
+    hq = synth.int8_codes(32, 2200, A, I)
+    ids = _skewed_rows(T, k, E, 32, hot=0)
+    offsets, srt, _ = oracle.sort(ids, E, tile)
+    cap = moe.moe_sort_tokens_capacity(T, k, E, tile)
+    srt_full = np.concatenate([srt, np.full(cap - srt.size, -1, np.int32)])
+    y = torch.full((A, H + 4), float("nan"), device="cuda")[:, :H]
+    moe.moe_mxfp4_down(dev(hq, 32), dev(hs), _stack(ex, E, "wd"), _stack(ex, E, "sd"), dev(offsets),
+                       dev(srt_full), T, k, y)
+    yo = np.empty((A, H))
+    for a in range(A):
+        e = ex[ids.ravel()[a]]
+        yo[a] = oracle.expert_down(hq[a], hs[a], e.wd, e.sd)
+    yg = host(y)
+    assert np.isfinite(yg).all()
+    assert max_err_over_rms(yg, yo) <= TOL
+    assert moe.moe_device_status() == 0
+
+
+def test_tensor_path_large_activations(moe):
+    """Activations far beyond the f16 range (|x| ~ 1.3e5): the per-token power
+    of two S_t keeps the f16 operands in [-1, 1], so the result is still the
+    oracle's within tolerance."""
+    spec = synth.LayerSpec(H=256, E=2, k=1, I=128, seed=33)
+    ex = {e: synth.expert(spec, e) for e in range(2)}
+    T = 20
+    xq = synth.int8_codes(33, 2300, T, 256)
+    xs = synth.positive_scales(33, 2301, T, 8, lo=200.0, hi=1000.0)
+    ids = np.zeros((T, 1), np.int32)
+    offsets, srt, _ = oracle.sort(ids, 2, 1)
+    W = {n: _stack(ex, 2, n) for n in ("wg", "sg", "wu", "su")}
+    h = torch.empty(T, 128, device="cuda")
+    moe.moe_mxfp4_gateup_swiglu(dev(xq), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets), dev(srt), 1, h)
+    ho = np.empty((T, 128))
+    for t in range(T):
+        g, u = oracle.expert_gateup(xq[t], xs[t], ex[0].wg, ex[0].sg, ex[0].wu, ex[0].su)
+        ho[t] = np.vectorize(oracle.silu)(g) * u
+    hg = host(h)
+    assert np.isfinite(hg).all()
+    assert max_err_over_rms(hg, ho) <= TOL
+    assert moe.moe_device_status() == 0
+
+
+def test_sixteen_rows_keep_the_exact_path(moe):
+    """16 rows take the CUDA-core path, 17 rows of the same data the tensor
+    path: on the 16 shared rows the two agree within the tolerance."""
+    H, I, E, k = 512, 256, 3, 2
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=34)
+    ex = {e: synth.expert(spec, e) for e in range(E)}
+    xq = synth.int8_codes(34, 2400, 17, H)
+    xs = synth.positive_scales(34, 2401, 17, H // 32)
+    ids = _skewed_rows(17, k, E, 34, hot=1)
+    W = {n: _stack(ex, E, n) for n in ("wg", "sg", "wu", "su")}
+    outs = {}
+    for T in (16, 17):
+        offsets, srt, _ = oracle.sort(ids[:T], E, 1)
+        h = torch.empty(T * k, I, device="cuda")
+        moe.moe_mxfp4_gateup_swiglu(dev(xq[:T]), dev(xs[:T]), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets),
+                                    dev(srt), k, h)
+        outs[T] = host(h)
+    assert max_err_over_rms(outs[17][: 16 * k], outs[16]) <= 2 * TOL
+    assert moe.moe_device_status() == 0
