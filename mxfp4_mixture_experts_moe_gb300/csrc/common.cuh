@@ -23,6 +23,7 @@ int sm_count();
 // with SwiGLU into out, nm = 1 down into out.  Used by the stage calls for
 // batches of more than kTensorMinRows - 1 rows.
 constexpr int kTensorMinRows = 17;
+bool tc_expert_supported(int K, int N);
 moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
                             const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
                             const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
