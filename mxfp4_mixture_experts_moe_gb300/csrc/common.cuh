@@ -174,6 +174,11 @@ MOE_DEVFN void cp_async4(uint32_t dst, const void *src) {
 MOE_DEVFN void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+MOE_DEVFN void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MOE_DEVFN void cp_async_wait() {  // at most N of this thread's committed groups still pending
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 MOE_DEVFN void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }

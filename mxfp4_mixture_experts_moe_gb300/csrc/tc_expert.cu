@@ -21,15 +21,25 @@
 // from the exact one by the tensor core's fp32 accumulation (relative
 // ~1e-5 on a 4096-term reduction) and B's residual.
 //
-// Tiles: 128 weight rows x up to 64 token columns of one expert, K in chunks
-// of 64 (two MX blocks); two MMAs (Bhi, Blo) per matrix and K step.  One
-// persistent CTA per SM walks the tile list it derives from the expert
-// offsets.  The packed weights of a chunk arrive by one 2-D tensor copy
-// (TMA) per matrix, the tile's scale bytes by one per matrix, the token rows
-// by cp.async, all into a deep raw ring; warps 0-7 widen them to f16 into an
-// operand ring in the tensor core's K-major core-matrix layout; warp 8
-// issues the MMAs; warps 0-3 also drain the accumulators (one TMEM lane
-// quadrant each).
+// Tiles: 128 weight rows x up to 32 token columns of one expert, K in chunks
+// of 64 (two MX blocks); two MMAs (Bhi, Blo) per matrix and K step, A read
+// from tensor memory.  One persistent CTA per SM walks the tile list it
+// derives from the expert offsets, with warp-specialised roles:
+//   warps 0-15  widen the packed weights of one row and 64 K to f16 in
+//               registers and store them into a tensor-memory operand stage
+//               (tcgen05.st), one lane per weight row, in groups that take
+//               alternate chunks;
+//   warps 16-19 copy the token rows ahead (cp.async ring), write Bhi / Blo
+//               into a shared-memory operand stage, and drain the previous
+//               tile's accumulators (one TMEM lane quadrant each);
+//   warp 20     issues the tensor copies (TMA): 128 weight rows x 128 bytes
+//               (256 K) per copy, 128-byte swizzled, and the tile's scale
+//               bytes into a double buffer;
+//   warp 21     issues the MMAs;
+//   warp 22     builds the next tile's column tables (assignment, activation
+//               row, S_t) ahead of time.
+// Tensor memory holds two accumulator buffers (the epilogue of one tile
+// overlaps the next) and the A operand stages.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,18 +51,27 @@
 namespace moe {
 namespace {
 
-constexpr int kTcRows = 128;   // weight rows per tile (MMA M)
-constexpr int kTcCols = 64;    // token columns per tile, at most (MMA N)
-constexpr int kTcK = 64;       // reduction elements per chunk
-constexpr int kTcRawMax = 12;  // packed-input stages, at most (as many as shared memory holds)
-constexpr int kTcF16Max = 4;   // f16 operand stages, at most
-constexpr int kTcConv = 8;     // converter warps
-constexpr int kTcThreads = (kTcConv + 1) * 32;
-constexpr int kConvThreads = kTcConv * 32;
-constexpr uint32_t kRawArow = 32;  // packed A row of a chunk (TMA box row)
-constexpr uint32_t kRawBrow = 80;  // B code row: 64 bytes, padded (conflict-free 8-byte reads)
-constexpr uint32_t kF16Mat = (uint32_t)kTcRows * kTcK * 2;  // one f16 A matrix tile, 16 KB
-constexpr uint32_t kF16B = (uint32_t)kTcCols * kTcK * 2;    // one f16 B tile (hi or lo), 8 KB
+constexpr int kTcRows = 128;    // weight rows per tile (MMA M)
+constexpr int kTcCols = 32;     // token columns per tile, at most (MMA N)
+constexpr int kTcK = 64;        // reduction elements per chunk (one operand stage)
+constexpr int kTcSlice = 256;   // reduction elements per packed-weight copy (128-byte rows)
+constexpr int kAWarps = 16;     // weight converters
+constexpr int kBWarps = 4;      // token side and epilogue
+constexpr int kWarpProd = kAWarps + kBWarps;
+constexpr int kWarpMma = kWarpProd + 1;
+constexpr int kWarpTab = kWarpMma + 1;
+constexpr int kTcThreads = 32 * (kWarpTab + 1);
+constexpr int kBThreads = 32 * kBWarps;
+constexpr int kBAhead = 6;      // token-row chunks in flight per token-side thread
+constexpr int kMaxA = 8;        // operand stages, at most
+constexpr int kMaxRaw = 8;      // packed-weight stages, at most
+constexpr uint32_t kRawMat = 128u * 128u;                     // one matrix's packed slice, 16 KB
+constexpr uint32_t kBStage = 2u * kTcCols * kTcK * 2u;        // Bhi + Blo of one chunk, 8 KB
+constexpr uint32_t kBRawSlot = (uint32_t)kBThreads * 20u;      // 16 code bytes + 1 scale per thread
+constexpr uint32_t kAccCols = 128;  // TMEM columns [0, 128): two accumulator buffers of 64
+constexpr uint32_t kTmemCols = 512;
+
+static_assert(kBThreads == 4 * kTcCols, "one token-side thread per (column, 16-element piece)");
 
 struct TcArgs {
   const int8_t *aq;  // Q8 activation codes: x rows (gate/up, by token) or h rows (down, by assignment)
@@ -68,52 +87,30 @@ struct TcArgs {
   int64_t ld_out;
   unsigned *status;
   int as16;  // activation scale rows are 16-byte aligned
-  // shared memory (bytes from the dynamic base)
-  uint32_t raw_stage, raw_b, raw_bs;  // raw stage size; B codes / B scales offsets in a stage
-  uint32_t f16_stage;                 // operand stage size (NM A tiles, then Bhi, Blo)
-  int nraw;                           // packed-input stages
-  int nf16;                           // operand stages
-  uint32_t off_raw, off_f16, off_scale, off_misc;
+  int nA;    // operand stages
+  int nraw;  // packed-weight stages
+  // shared memory (bytes from the 1024-aligned base)
+  uint32_t scale_buf;  // one tile's scale bytes (NM x 128 rows x K/32)
+  uint32_t off_scale, off_raw, off_b, off_braw, off_misc;
 };
 
 struct TcMaps {  // 2-D tensor maps (TMA) of the packed weights and their scale bytes
   CUtensorMap w[2], s[2];
 };
 
-struct TcMisc {  // small shared state
-  uint64_t *raw_full, *f16_full, *f16_empty, *acc_full, *acc_empty, *scale_full;
-  uint32_t *tmem_slot;
-  int *prefix;   // [E+1] tiles before expert e
-  int *colrow;   // [64] activation row of each token column (-1: padding)
-  int *colasg;   // [64] assignment of each column (-1: padding)
-  int *umax;     // [2][128] largest scale byte of each weight row
-  float *colS;   // [64] token scale S_t (a power of two)
-  float *colInv; // [64] 1 / S_t
+struct TcShared {
+  uint64_t raw_full[kMaxRaw], raw_empty[kMaxRaw];
+  uint64_t full[kMaxA], a_empty[kMaxA];
+  uint64_t acc_full[2], acc_empty[2], scale_full[2], scale_empty[2], tab_full[2], tab_empty[2], umax_full[3];
+  uint32_t tmem_slot;
+  int ncols[2], mtile[2];
+  int colrow[2][kTcCols], colasg[2][kTcCols];
+  float colS[2][kTcCols], colInv[2][kTcCols];
+  int umax[3][2 * kTcRows];  // largest scale byte of each weight row (matrix-major)
+  int prefix[1];             // [E + 1] tiles before expert e
 };
 
-MOE_DEVFN TcMisc tc_misc(uint8_t *base) {
-  TcMisc m;
-  uint64_t *b = reinterpret_cast<uint64_t *>(base);
-  m.raw_full = b; b += kTcRawMax;
-  m.f16_full = b; b += kTcF16Max;
-  m.f16_empty = b; b += kTcF16Max;
-  m.acc_full = b; b += 1;
-  m.acc_empty = b; b += 1;
-  m.scale_full = b; b += 1;
-  uint32_t *w = reinterpret_cast<uint32_t *>(b);
-  m.tmem_slot = w; w += 4;
-  m.colrow = reinterpret_cast<int *>(w); w += kTcCols;
-  m.colasg = reinterpret_cast<int *>(w); w += kTcCols;
-  m.umax = reinterpret_cast<int *>(w); w += 2 * kTcRows;
-  m.colS = reinterpret_cast<float *>(w); w += kTcCols;
-  m.colInv = reinterpret_cast<float *>(w); w += kTcCols;
-  m.prefix = reinterpret_cast<int *>(w);
-  return m;
-}
-
-uint32_t tc_misc_bytes(int E) {
-  return 8u * (kTcRawMax + 2 * kTcF16Max + 3) + 4u * (4 + 4 * kTcCols + 2 * kTcRows) + 4u * (E + 1);
-}
+uint32_t tc_shared_bytes(int E) { return (uint32_t)(sizeof(TcShared) + 4u * (uint32_t)E); }
 
 // f16 bits of 2^-d (d >= 0): normal down to 2^-14, subnormal to 2^-24, else 0.
 MOE_DEVFN uint32_t f16_pow2_neg(int d) {
@@ -138,6 +135,27 @@ MOE_DEVFN float pow2_ceil(float v) {
   return __uint_as_float((e + (man != 0)) << 23);
 }
 
+MOE_DEVFN uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// A box of 128 rows x nb bytes lands in shared memory with the tensor-copy
+// swizzle that matches its row length (nb = 128 / 64 / 32 bytes: 128B / 64B /
+// 32B swizzle, 16: none): the 16-byte chunk j of row r sits at chunk j ^ x(r).
+MOE_DEVFN uint32_t swz_of(int r, int nb) {
+  return nb == 128 ? (uint32_t)(r & 7) : nb == 64 ? (uint32_t)((r >> 1) & 3) : nb == 32 ? (uint32_t)((r >> 2) & 1) : 0u;
+}
+MOE_DEVFN uint32_t swz_addr(uint32_t base, int r, int byte, int nb, uint32_t x) {
+  return base + (uint32_t)r * (uint32_t)nb + ((((uint32_t)byte >> 4) ^ x) << 4) + ((uint32_t)byte & 15u);
+}
+
+// Bounded mbarrier wait taken by a whole warp, with one answer for all lanes.
+MOE_DEVFN bool warp_wait(uint32_t bar, uint32_t parity, unsigned *status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
 // 2-D tensor copy of one box into shared memory, completing on bar.
 MOE_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -152,17 +170,17 @@ struct Tile {
   int col0;      // first sorted position of the tile
 };
 
-MOE_DEVFN Tile tile_of(const TcMisc &m, const TcArgs &p, int t, int mt) {
+MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   // expert: last e with prefix[e] <= t (binary search over E+1 entries)
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (m.prefix[mid] <= t) lo = mid;
+    if (S.prefix[mid] <= t) lo = mid;
     else hi = mid;
   }
   Tile tl;
   tl.e = lo;
-  const int local = t - m.prefix[lo];
+  const int local = t - S.prefix[lo];
   tl.mtile = local % mt;
   const int ntile = local / mt;
   const int b = p.offsets[lo], n_e = p.offsets[lo + 1] - b;
@@ -173,62 +191,55 @@ MOE_DEVFN Tile tile_of(const TcMisc &m, const TcArgs &p, int t, int mt) {
   return tl;
 }
 
-// One chunk of the packed inputs into a raw stage: the weights by tensor copy
-// (thread 0, expect_tx on the stage barrier), the token rows by cp.async from
-// every converter thread (each then arrives on the barrier when its copies land).
-template <int NM>
-MOE_DEVFN void issue_raw(const TcArgs &p, const TcMaps &maps, const TcMisc &m, const Tile &tl, uint32_t raw,
-                         uint32_t bar, int chunk, int ct) {
-  const int k0 = chunk * kTcK;
-  if (ct == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)NM * kTcRows * kRawArow);
+// Four packed bytes (8 weights) -> four f16x2 pairs scaled by f2.
+MOE_DEVFN void widen8(uint32_t w, uint32_t f2, uint32_t *o) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
 #pragma unroll
-    for (int mm = 0; mm < NM; ++mm)
-      tma_load_2d(raw + (uint32_t)mm * kTcRows * kRawArow, &maps.w[mm], k0 / 2, (int)tl.row0, bar);
-  }
-  for (int q = ct; q < tl.ncol16 * 4; q += kConvThreads) {
-    const int c = q >> 2, part = q & 3;
-    const uint32_t dst = raw + p.raw_b + (uint32_t)c * kRawBrow + 16u * part;
-    const int row = m.colrow[c];
-    if (row >= 0) cp_async16(dst, p.aq + (int64_t)row * p.ld_aq + k0 + 16 * part);
-    else sts128(dst, make_uint4(0, 0, 0, 0));
-  }
-  for (int q = ct; q < tl.ncol16 * 2; q += kConvThreads) {
-    const int c = q >> 1, j = q & 1;
-    const uint32_t dst = raw + p.raw_bs + (uint32_t)c * 8u + 4u * j;
-    const int row = m.colrow[c];
-    if (row >= 0) cp_async4(dst, p.as + (int64_t)row * p.ld_as + k0 / 32 + j);
-    else sts32(dst, 0u);
-  }
-  cp_async_mbar_arrive_noinc(bar);
+  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(f2));
 }
 
 template <int NM>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p, const __grid_constant__ TcMaps maps) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  const uint32_t dyn = smem_addr(smem_dyn);
+  const uint32_t pad = ((dyn + 1023u) & ~1023u) - dyn;
+  uint8_t *smem = smem_dyn + pad;
+  const uint32_t sb = dyn + pad;
+  TcShared &S = *reinterpret_cast<TcShared *>(smem + p.off_misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int K = p.K, nb = K / 32, nchunk = K / kTcK, mt = p.N / kTcRows;
-  const TcMisc m = tc_misc(smem + p.off_misc);
-  const uint32_t sraw = smem_addr(smem + p.off_raw), sf16 = smem_addr(smem + p.off_f16);
-  const uint32_t sscale = smem_addr(smem + p.off_scale);
+  const int K = p.K, nb = K / 32, nchunk = K / kTcK, nslice = K / kTcSlice, mt = p.N / kTcRows;
+  const int nA = p.nA, nraw = p.nraw;
+  constexpr int NG = 4 / NM;  // converter groups (chunks c = group mod NG)
 
   if (tid == 0) {
-    for (int s = 0; s < p.nraw; ++s) mbar_init(smem_addr(&m.raw_full[s]), kConvThreads + 1);
-    for (int s = 0; s < p.nf16; ++s) {
-      mbar_init(smem_addr(&m.f16_full[s]), kConvThreads);
-      mbar_init(smem_addr(&m.f16_empty[s]), 1);
+    for (int s = 0; s < nraw; ++s) {
+      mbar_init(smem_addr(&S.raw_full[s]), 1);
+      mbar_init(smem_addr(&S.raw_empty[s]), kAWarps);
     }
-    mbar_init(smem_addr(m.acc_full), 1);
-    mbar_init(smem_addr(m.acc_empty), 4);
-    mbar_init(smem_addr(m.scale_full), 1);
+    for (int s = 0; s < nA; ++s) {
+      mbar_init(smem_addr(&S.full[s]), 4 * NM + kBWarps);
+      mbar_init(smem_addr(&S.a_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&S.acc_full[b]), 1);
+      mbar_init(smem_addr(&S.acc_empty[b]), kBWarps);
+      mbar_init(smem_addr(&S.scale_full[b]), 1);
+      mbar_init(smem_addr(&S.scale_empty[b]), kAWarps);
+      mbar_init(smem_addr(&S.tab_full[b]), 1);
+      mbar_init(smem_addr(&S.tab_empty[b]), kBWarps);
+    }
+    for (int b = 0; b < 3; ++b) mbar_init(smem_addr(&S.umax_full[b]), 4 * NM);
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(smem_addr(m.tmem_slot), NM * kTcRows);
+  if (warp == kWarpTab) {
     // tiles per expert, prefix-summed (every CTA derives the same list)
     int carry = 0;
-    if (lane == 0) m.prefix[0] = 0;
+    if (lane == 0) S.prefix[0] = 0;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + lane;
       int nt = 0;
@@ -244,167 +255,158 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (e < p.E) m.prefix[e + 1] = carry + incl;
+      if (e < p.E) S.prefix[e + 1] = carry + incl;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  if (warp == 0) tmem_alloc(smem_addr(&S.tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(m.tmem_slot);
-  const int ntiles = m.prefix[p.E];
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&S.tmem_slot);
+  const int ntiles = S.prefix[p.E];
+  const int my_tiles = cta < ntiles ? (ntiles - cta + G - 1) / G : 0;
+  const uint32_t s_scale = sb + p.off_scale, s_raw = sb + p.off_raw, s_b = sb + p.off_b, s_braw = sb + p.off_braw;
 
-  if (warp == kTcConv) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const int nf16 = p.nf16;
-      int g = 0, done = 0;
-      for (int t = cta; t < ntiles; t += G) {
-        const Tile tl = tile_of(m, p, t, mt);
-        const uint32_t idesc = idesc_f16(kTcRows, tl.ncol16);
-        if (done > 0 && !mbar_wait(smem_addr(m.acc_empty), (done - 1) & 1, p.status)) break;
-        tc_fence_after();
-        bool ok = true;
-        for (int c = 0; c < nchunk; ++c, ++g) {
-          const int s = g % nf16;
-          if (!mbar_wait(smem_addr(&m.f16_full[s]), (g / nf16) & 1, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = sf16 + (uint32_t)s * p.f16_stage;
-#pragma unroll
-          for (int mm = 0; mm < NM; ++mm) {
-#pragma unroll
-            for (int ks = 0; ks < kTcK / 16; ++ks) {
-              const uint64_t ad = smem_desc(st + mm * kF16Mat + 256u * ks, kCoreLbo, kCoreSbo);
-              mma_f16(tmem + (uint32_t)mm * kTcRows, ad, smem_desc(st + NM * kF16Mat + 256u * ks, kCoreLbo, kCoreSbo),
-                      idesc, c > 0 || ks > 0);
-              mma_f16(tmem + (uint32_t)mm * kTcRows, ad,
-                      smem_desc(st + NM * kF16Mat + kF16B + 256u * ks, kCoreLbo, kCoreSbo), idesc, true);
-            }
-          }
-          mma_commit(smem_addr(&m.f16_empty[s]));
-        }
-        if (!ok) break;
-        mma_commit(smem_addr(m.acc_full));
-        ++done;
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ converters
-  const int ct = tid;  // 0 .. kConvThreads-1
-  const int nraw = p.nraw, nf16 = p.nf16;
-  int g = 0, done = 0;
-  bool dead = false;
-  for (int t = cta; t < ntiles && !dead; t += G) {
-    const Tile tl = tile_of(m, p, t, mt);
-    // the tile's scale bytes (NM x 128 rows x nb) by tensor copy
-    if (ct == 0) {
-      mbar_arrive_expect_tx(smem_addr(m.scale_full), (uint32_t)NM * kTcRows * nb);
-#pragma unroll
-      for (int mm = 0; mm < NM; ++mm)
-        tma_load_2d(sscale + (uint32_t)mm * kTcRows * nb, &maps.s[mm], 0, (int)tl.row0, smem_addr(m.scale_full));
-    }
-    // columns: activation row and assignment of each token column
-    for (int c = ct; c < kTcCols; c += kConvThreads) {
-      int a = -1;
-      if (c < tl.ncols) {
-        a = p.sorted[tl.col0 + c];
-        if (a >= p.A) {
-          if (p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-          a = -1;
-        }
-      }
-      m.colasg[c] = a;
-      m.colrow[c] = a < 0 ? -1 : (p.bytoken ? token_of(a, p.kdiv) : a);
-    }
-    bar_sync_named(1, kConvThreads);  // the column tables are read by other threads below
-    // prologue: the first raw chunks (the scale copy is already on its way)
-    for (int j = 0; j < nraw && j < nchunk; ++j)
-      issue_raw<NM>(p, maps, m, tl, sraw + (uint32_t)((g + j) % nraw) * p.raw_stage,
-                    smem_addr(&m.raw_full[(g + j) % nraw]), j, ct);
-    // each token column's scale S_t: two threads per column, half the row's block scales each
-    if (ct < 2 * kTcCols) {
-      const int c = ct >> 1, half = ct & 1;
-      const int row = m.colrow[c];
-      float mx = 0.0f;
-      if (row >= 0) {
-        const float *sp = p.as + (int64_t)row * p.ld_as + half * (nb / 2);
-        if (p.as16) {
-          const float4 *s4 = reinterpret_cast<const float4 *>(sp);
-          for (int w = 0; w < nb / 8; ++w) {
-            const float4 v = __ldg(s4 + w);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-          }
-        } else {
-          for (int w = 0; w < nb / 2; ++w) mx = fmaxf(mx, fabsf(__ldg(sp + w)));
-        }
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      if (half == 0) {
-        // |q * sx| <= 127 * max sx; S_t scales the column into [-2^15, 2^15],
-        // the top of the f16 normal range, so that blocks far below the
-        // column's largest stay normal (full 11-bit precision in Bhi and Blo)
-        const float S = __fmul_rn(pow2_ceil(127.0f * mx), 1.0f / 32768.0f);
-        m.colS[c] = S;
-        m.colInv[c] = 1.0f / S;
-      }
-    }
-    // each weight row's largest scale byte
-    if (!mbar_wait(smem_addr(m.scale_full), done & 1, p.status)) dead = true;
-    if (ct < NM * kTcRows) {
+  if (warp < kAWarps) {
+    // ------------------------------------------------ weights -> tensor memory
+    const int grp = warp / (4 * NM), mm = NM == 2 ? (warp >> 2) & 1 : 0, q = warp & 3;
+    const int r = 32 * q + lane;  // weight row of the tile = TMEM lane
+    const uint32_t lanes = (uint32_t)(32 * q) << 16;
+    const uint32_t xs = swz_of(r, nb), xr = (uint32_t)(r & 7);
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const int sbuf = lt & 1;
+      const uint32_t scl = s_scale + (uint32_t)sbuf * p.scale_buf + (uint32_t)mm * kTcRows * nb;
+      if (!warp_wait(smem_addr(&S.scale_full[sbuf]), (lt >> 1) & 1, p.status)) break;
       uint32_t m4 = 0;
-      for (int w = 0; w < nb / 16; ++w) {
-        const uint4 v = lds128(sscale + (uint32_t)ct * nb + 16u * w);
+      for (int j = 0; j < nb / 16; ++j) {
+        const uint4 v = lds128(swz_addr(scl, r, 16 * j, nb, xs));
         m4 = __vmaxu4(__vmaxu4(m4, v.x), __vmaxu4(__vmaxu4(v.y, v.z), v.w));
       }
-      m.umax[ct] = (int)max(max(m4 & 0xFFu, (m4 >> 8) & 0xFFu), max((m4 >> 16) & 0xFFu, m4 >> 24));
+      const int umax = (int)max(max(m4 & 0xFFu, (m4 >> 8) & 0xFFu), max((m4 >> 16) & 0xFFu, m4 >> 24));
+      if (grp == 0) {
+        S.umax[lt % 3][mm * kTcRows + r] = umax;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&S.umax_full[lt % 3]));
+      }
+      bool dead = false;
+      for (int c = grp; c < nchunk; c += NG) {
+        const int g = lt * nchunk + c, s = g % nA;
+        const int J = lt * nslice + (c >> 2), rs = J % nraw;
+        if (!warp_wait(smem_addr(&S.raw_full[rs]), (J / nraw) & 1, p.status)) { dead = true; break; }
+        if (g >= nA && !warp_wait(smem_addr(&S.a_empty[s]), ((g / nA) - 1) & 1, p.status)) { dead = true; break; }
+        tc_fence_after();
+        const uint32_t row = s_raw + (uint32_t)rs * NM * kRawMat + (uint32_t)mm * kRawMat + (uint32_t)r * 128u;
+        const uint32_t j0 = 2u * (uint32_t)(c & 3);
+        const uint4 pa = lds128(row + ((j0 ^ xr) << 4));
+        const uint4 pb = lds128(row + (((j0 + 1u) ^ xr) << 4));
+        const uint32_t u2 = lds_u16(swz_addr(scl, r, 2 * c, nb, xs));
+        const uint32_t fa = f16_pow2_neg(umax - (int)(u2 & 0xFFu)), fb = f16_pow2_neg(umax - (int)(u2 >> 8));
+        const uint32_t fa2 = fa | (fa << 16), fb2 = fb | (fb << 16);
+        uint32_t o[32];
+        widen8(pa.x, fa2, o + 0);
+        widen8(pa.y, fa2, o + 4);
+        widen8(pa.z, fa2, o + 8);
+        widen8(pa.w, fa2, o + 12);
+        widen8(pb.x, fb2, o + 16);
+        widen8(pb.y, fb2, o + 20);
+        widen8(pb.z, fb2, o + 24);
+        widen8(pb.w, fb2, o + 28);
+        tmem_st32(tmem + lanes + kAccCols + (uint32_t)(s * NM + mm) * 32u, o);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&S.full[s]));
+          if ((c & 3) + NG >= 4) mbar_arrive(smem_addr(&S.raw_empty[rs]));  // this group's last chunk of the slice
+        }
+      }
+      if (dead) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.scale_empty[sbuf]));
     }
-    bar_sync_named(1, kConvThreads);
-    for (int c = 0; c < nchunk; ++c, ++g) {
-      const int rs = g % nraw, s = g % nf16;
-      const uint32_t raw = sraw + (uint32_t)rs * p.raw_stage;
-      const uint32_t st = sf16 + (uint32_t)s * p.f16_stage;
-      if (!mbar_wait(smem_addr(&m.raw_full[rs]), (g / nraw) & 1, p.status)) dead = true;
-      if (g >= nf16 && !mbar_wait(smem_addr(&m.f16_empty[s]), ((g / nf16) - 1) & 1, p.status)) dead = true;
-      if (!dead) {
-        // A: (matrix, row, half) -> 32 weights of one MX block, scaled by 2^(u - umax)
+  } else if (warp < kWarpProd) {
+    // ------------------------------------------------ token side + epilogue
+    const int bt = tid - 32 * kAWarps, q = warp & 3;
+    const int cc = bt >> 2, pc = bt & 3;  // token column, 16-element piece of the chunk
+    const int total = my_tiles * nchunk;
+    bool dead = false;
+    auto issue = [&](int pos) {
+      if (pos < total) {
+        const int lt = pos / nchunk, c = pos - lt * nchunk, tb = lt & 1;
+        if (c == 0 && !warp_wait(smem_addr(&S.tab_full[tb]), (lt >> 1) & 1, p.status)) dead = true;
+        const int row = dead ? -1 : S.colrow[tb][cc];
+        if (row >= 0) {
+          const uint32_t slot = s_braw + (uint32_t)(pos % kBAhead) * kBRawSlot;
+          cp_async16(slot + 16u * bt, p.aq + (int64_t)row * p.ld_aq + c * kTcK + 16 * pc);
+          cp_async4(slot + 16u * kBThreads + 4u * bt, p.as + (int64_t)row * p.ld_as + 2 * c + (pc >> 1));
+        }
+      }
+      cp_async_commit();
+    };
+    auto epilogue = [&](int lt) {
+      const int ab = lt & 1, tb = lt & 1, u3 = lt % 3;
+      bool ok = warp_wait(smem_addr(&S.acc_full[ab]), (lt >> 1) & 1, p.status) &&
+                warp_wait(smem_addr(&S.umax_full[u3]), (lt / 3) & 1, p.status);
+      tc_fence_after();
+      const int i = 32 * q + lane;
+      const float rs0 = e8m0_value(S.umax[u3][i]);
+      const float rs1 = NM == 2 ? e8m0_value(S.umax[u3][kTcRows + i]) : 0.0f;
+      const int ncols = S.ncols[tb], ncol16 = (ncols + 15) & ~15;
+      const int64_t orow = (int64_t)S.mtile[tb] * kTcRows + i;
+      const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * 64u;
+      for (int cb = 0; ok && cb < ncol16; cb += 16) {
+        float d0[16];
+        tmem_ld16(acc + (uint32_t)cb, d0);
+        if (NM == 2) {
+          float d1[16];
+          tmem_ld16(acc + 32u + (uint32_t)cb, d1);
 #pragma unroll
-        for (int j = 0; j < NM; ++j) {
-          const int q = ct + kConvThreads * j;
-          const int mm = q >> 8, r = q & 127, h = (q >> 7) & 1;
-          const uint4 pk = lds128(raw + (uint32_t)mm * kTcRows * kRawArow + (uint32_t)r * kRawArow + 16u * h);
-          const int u = (int)lds_u8(sscale + (uint32_t)(mm * kTcRows + r) * nb + 2 * c + h);
-          const uint32_t f1 = f16_pow2_neg(m.umax[mm * kTcRows + r] - u);
-          const uint32_t f2 = f1 | (f1 << 16);
-          const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
+          for (int j = 0; j < 16; ++j) {
+            const int col = cb + j;
+            const int a = col < ncols ? S.colasg[tb][col] : -1;
+            if (a >= 0) {
+              const float Sc = S.colS[tb][col];
+              const float gv = __fmul_rn(__fmul_rn(d0[j], rs0), Sc), uv = __fmul_rn(__fmul_rn(d1[j], rs1), Sc);
+              p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(silu(gv), uv);
+            }
+          }
+        } else {
 #pragma unroll
-          for (int wd = 0; wd < 4; ++wd) {
-            uint32_t o[4];
-            asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-                " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-                " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-                : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-                : "r"(pw[wd]));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(f2));
-            sts128(st + (uint32_t)mm * kF16Mat + tile_offset(r, 32 * h + 8 * wd), make_uint4(o[0], o[1], o[2], o[3]));
+          for (int j = 0; j < 16; ++j) {
+            const int col = cb + j;
+            const int a = col < ncols ? S.colasg[tb][col] : -1;
+            if (a >= 0) p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(__fmul_rn(d0[j], rs0), S.colS[tb][col]);
           }
         }
-        // B: (column, group of 8) -> v = q * sx / S_t as f16 hi + lo
-        for (int q = ct; q < tl.ncol16 * 8; q += kConvThreads) {
-          const int cc = q % tl.ncol16, grp = q / tl.ncol16;
-          uint2 codes;
-          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(codes.x), "=r"(codes.y)
-                       : "r"(raw + p.raw_b + (uint32_t)cc * kRawBrow + 8u * grp));
-          const float fac = __fmul_rn(lds_f32(raw + p.raw_bs + (uint32_t)cc * 8u + 4u * (grp >> 2)), m.colInv[cc]);
-          uint32_t hi[4], lo[4];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&S.acc_empty[ab]));
+        mbar_arrive(smem_addr(&S.tab_empty[tb]));
+      }
+      return ok;
+    };
+    for (int j = 0; j < kBAhead - 1; ++j) issue(j);
+    for (int pos = 0; pos < total && !dead; ++pos) {
+      issue(pos + kBAhead - 1);
+      cp_async_wait<kBAhead - 1>();
+      const int lt = pos / nchunk, c = pos - lt * nchunk, tb = lt & 1;
+      const int s = pos % nA;
+      if (pos >= nA && !warp_wait(smem_addr(&S.a_empty[s]), ((pos / nA) - 1) & 1, p.status)) break;
+      const int ncols = S.ncols[tb], ncol16 = (ncols + 15) & ~15;
+      if (cc < ncol16) {
+        uint32_t hi[8], lo[8];
+        const int row = S.colrow[tb][cc];
+        if (cc < ncols && row >= 0) {
+          const uint32_t slot = s_braw + (uint32_t)(pos % kBAhead) * kBRawSlot;
+          const uint4 codes = lds128(slot + 16u * bt);
+          const float fac = __fmul_rn(lds_f32(slot + 16u * kBThreads + 4u * bt), S.colInv[tb][cc]);
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t wv = i < 2 ? codes.x : codes.y;
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t wv = cw[i >> 1];
             const int sh = 16 * (i & 1);
             const float v0 = __fmul_rn((float)(int8_t)(wv >> sh), fac);
             const float v1 = __fmul_rn((float)(int8_t)(wv >> (sh + 8)), fac);
@@ -414,60 +416,143 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
                 : "=f"(h0), "=f"(h1) : "r"(hi[i]));
             asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo[i]) : "f"(__fsub_rn(v1, h1)), "f"(__fsub_rn(v0, h0)));
           }
-          const uint32_t off = tile_offset(cc, 8 * grp);
-          sts128(st + NM * kF16Mat + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-          sts128(st + NM * kF16Mat + kF16B + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(smem_addr(&m.f16_full[s]));
-      bar_sync_named(1, kConvThreads);  // every converter is done with raw stage rs
-      if (c + nraw < nchunk) issue_raw<NM>(p, maps, m, tl, raw, smem_addr(&m.raw_full[rs]), c + nraw, ct);
-    }
-    // ---------------------------------------------------------- epilogue
-    if (warp < 4) {
-      const bool ok = !dead && mbar_wait(smem_addr(m.acc_full), done & 1, p.status);
-      tc_fence_after();
-      const int i = 32 * warp + lane;  // weight row in the tile = TMEM lane
-      const float rs0 = e8m0_value(m.umax[i]);
-      const float rs1 = NM == 2 ? e8m0_value(m.umax[kTcRows + i]) : 0.0f;
-      const int64_t orow = (int64_t)tl.mtile * kTcRows + i;
-      for (int cb = 0; ok && cb < tl.ncol16; cb += 32) {
-        float d0[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)cb, d0);
-        if (NM == 2) {
-          float d1[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(kTcRows + cb), d1);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = cb + j;
-            const int a = col < tl.ncols ? m.colasg[col] : -1;
-            if (a >= 0) {
-              const float S = m.colS[col];
-              const float gv = __fmul_rn(__fmul_rn(d0[j], rs0), S), uv = __fmul_rn(__fmul_rn(d1[j], rs1), S);
-              p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(silu(gv), uv);
-            }
-          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = cb + j;
-            const int a = col < tl.ncols ? m.colasg[col] : -1;
-            if (a >= 0) p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(__fmul_rn(d0[j], rs0), m.colS[col]);
+          for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0u;
+        }
+        const uint32_t st = s_b + (uint32_t)s * kBStage;
+        const uint32_t o0 = tile_offset(cc, 16 * pc), o1 = tile_offset(cc, 16 * pc + 8);
+        sts128(st + o0, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+        sts128(st + o1, make_uint4(hi[4], hi[5], hi[6], hi[7]));
+        sts128(st + kBStage / 2 + o0, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        sts128(st + kBStage / 2 + o1, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.full[s]));
+      // the previous tile's accumulators, once this tile's first chunks are on their way
+      if (lt >= 1 && c == min(1, nchunk - 1) && !epilogue(lt - 1)) dead = true;
+    }
+    cp_async_wait<0>();
+    if (!dead && my_tiles > 0) epilogue(my_tiles - 1);
+  } else if (warp == kWarpProd) {
+    // ------------------------------------------------ tensor copies
+    if (lane == 0) {
+      int J = 0;
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const Tile tl = tile_of(S, p, cta + lt * G, mt);
+        const int sbuf = lt & 1;
+        if (lt >= 2 && !mbar_wait(smem_addr(&S.scale_empty[sbuf]), ((lt >> 1) - 1) & 1, p.status)) break;
+        const uint32_t sbar = smem_addr(&S.scale_full[sbuf]);
+        mbar_arrive_expect_tx(sbar, (uint32_t)NM * kTcRows * nb);
+#pragma unroll
+        for (int mm = 0; mm < NM; ++mm)
+          tma_load_2d(s_scale + (uint32_t)sbuf * p.scale_buf + (uint32_t)mm * kTcRows * nb, &maps.s[mm], 0,
+                      (int)tl.row0, sbar);
+        bool dead = false;
+        for (int sl = 0; sl < nslice; ++sl, ++J) {
+          const int rs = J % nraw;
+          if (J >= nraw && !mbar_wait(smem_addr(&S.raw_empty[rs]), ((J / nraw) - 1) & 1, p.status)) {
+            dead = true;
+            break;
           }
+          const uint32_t bar = smem_addr(&S.raw_full[rs]);
+          mbar_arrive_expect_tx(bar, (uint32_t)NM * kRawMat);
+#pragma unroll
+          for (int mm = 0; mm < NM; ++mm)
+            tma_load_2d(s_raw + (uint32_t)(rs * NM + mm) * kRawMat, &maps.w[mm], sl * 128, (int)tl.row0, bar);
+        }
+        if (dead) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------ MMA issue
+    if (lane == 0) {
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const Tile tl = tile_of(S, p, cta + lt * G, mt);
+        const int ab = lt & 1;
+        if (lt >= 2 && !mbar_wait(smem_addr(&S.acc_empty[ab]), ((lt >> 1) - 1) & 1, p.status)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16(kTcRows, tl.ncol16);
+        bool ok = true;
+        for (int c = 0; c < nchunk; ++c) {
+          const int g = lt * nchunk + c, s = g % nA;
+          if (!mbar_wait(smem_addr(&S.full[s]), (g / nA) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t bh = s_b + (uint32_t)s * kBStage, bl = bh + kBStage / 2;
+#pragma unroll
+          for (int mm = 0; mm < NM; ++mm) {
+            const uint32_t d = tmem + (uint32_t)ab * 64u + (uint32_t)mm * 32u;
+            const uint32_t a = tmem + kAccCols + (uint32_t)(s * NM + mm) * 32u;
+#pragma unroll
+            for (int ks = 0; ks < kTcK / 16; ++ks) {
+              mma_f16_ts(d, a + 8u * ks, smem_desc(bh + 256u * ks, kCoreLbo, kCoreSbo), idesc, c > 0 || ks > 0);
+              mma_f16_ts(d, a + 8u * ks, smem_desc(bl + 256u * ks, kCoreLbo, kCoreSbo), idesc, true);
+            }
+          }
+          mma_commit(smem_addr(&S.a_empty[s]));
+        }
+        if (!ok) break;
+        mma_commit(smem_addr(&S.acc_full[ab]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ column tables, one tile ahead
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const Tile tl = tile_of(S, p, cta + lt * G, mt);
+      const int tb = lt & 1;
+      if (lt >= 2 && !warp_wait(smem_addr(&S.tab_empty[tb]), ((lt >> 1) - 1) & 1, p.status)) break;
+      const int c = lane;
+      int a = -1;
+      if (c < tl.ncols) {
+        a = p.sorted[tl.col0 + c];  // -1: padding of the expert's segment
+        if (a >= p.A) {
+          if (p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+          a = -1;
         }
       }
-      tc_fence_before();
+      const int row = a < 0 ? -1 : (p.bytoken ? token_of(a, p.kdiv) : a);
+      // the column's scale S_t: |q * sx| <= 127 * max sx; S_t scales the
+      // column into [-2^15, 2^15], the top of the f16 normal range, so that
+      // blocks far below the column's largest stay normal (full 11-bit
+      // precision in Bhi and Blo)
+      float mx = 0.0f;
+      if (row >= 0) {
+        const float *sp = p.as + (int64_t)row * p.ld_as;
+        if (p.as16) {
+          const float4 *s4 = reinterpret_cast<const float4 *>(sp);
+          for (int w = 0; w < nb / 4; ++w) {
+            const float4 v = __ldg(s4 + w);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+          }
+        } else {
+          for (int w = 0; w < nb; ++w) mx = fmaxf(mx, fabsf(__ldg(sp + w)));
+        }
+      }
+      const float Sc = __fmul_rn(pow2_ceil(127.0f * mx), 1.0f / 32768.0f);
+      S.colasg[tb][c] = a;
+      S.colrow[tb][c] = row;
+      S.colS[tb][c] = Sc;
+      S.colInv[tb][c] = 1.0f / Sc;
+      if (lane == 0) {
+        S.ncols[tb] = tl.ncols;
+        S.mtile[tb] = tl.mtile;
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(m.acc_empty));
+      if (lane == 0) mbar_arrive(smem_addr(&S.tab_full[tb]));
     }
-    ++done;
-    bar_sync_named(1, kConvThreads);  // the epilogue is done with this tile's tables
   }
-  // all MMAs of this CTA have completed (the last epilogue waited for them)
+  // every MMA of this CTA has completed (the last epilogue waited for it)
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, NM * kTcRows);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -485,7 +570,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Row-major u8 matrix [rows][cols] (cols bytes per row) as a 2-D tensor map
-// with boxes of box_cols bytes x 128 rows.
+// with boxes of box_cols bytes x 128 rows, swizzled to match box_cols.
 bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -493,14 +578,18 @@ bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t col
   const cuuint64_t strides[1] = {cols};
   const cuuint32_t box[2] = {box_cols, (cuuint32_t)kTcRows};
   const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle swz = box_cols == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-bool tc_expert_supported(int K, int N) { return K % 512 == 0 && K <= 8192 && N % kTcRows == 0; }
+bool tc_expert_supported(int K, int N) { return K % 512 == 0 && K <= 4096 && N % kTcRows == 0; }
 
 // Launch of the tensor-core path (moe_mxfp4_gateup_swiglu / moe_mxfp4_down for
 // T > 16).  nm = 2: gate and up with SwiGLU; nm = 1: down.
@@ -510,7 +599,7 @@ moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float
                             int K, int N, int bytoken, float *out, int64_t ld_out, cudaStream_t stream,
                             const char *name) {
   if (!tc_expert_supported(K, N))
-    return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs K %% 512 == 0 (<= 8192) and rows %% 128 == 0", name);
+    return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs K %% 512 == 0 (<= 4096) and rows %% 128 == 0", name);
   if (E > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d", name, E);
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -528,33 +617,36 @@ moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float
   TcMaps maps{};
   const uint64_t rows = (uint64_t)E * N;
   for (int mm = 0; mm < nm; ++mm) {
-    if (!encode_rows(&maps.w[mm], mm == 0 ? w0 : w1, rows, (uint64_t)K / 2, kRawArow) ||
+    if (!encode_rows(&maps.w[mm], mm == 0 ? w0 : w1, rows, (uint64_t)K / 2, 128u) ||
         !encode_rows(&maps.s[mm], mm == 0 ? s0 : s1, rows, (uint64_t)K / 32, (uint32_t)(K / 32)))
       return fail(MOE_ERR_UNSUPPORTED, "%s: tensor maps of the weights could not be built (16-byte aligned weights and scales are required)", name);
   }
-  p.raw_b = (uint32_t)nm * kTcRows * kRawArow;
-  p.raw_bs = p.raw_b + (uint32_t)kTcCols * kRawBrow;
-  p.raw_stage = (p.raw_bs + (uint32_t)kTcCols * 8u + 127u) & ~127u;
-  p.f16_stage = (uint32_t)nm * kF16Mat + 2 * kF16B;
-  // operand stages first (deep enough to cover the MMA round trip), then the
-  // tile's scales, then as many packed-input stages as shared memory holds
-  const uint32_t scale_bytes = ((uint32_t)nm * kTcRows * (K / 32) + 127u) & ~127u;
-  const size_t misc = tc_misc_bytes(E) + 128;
-  int nf16 = kTcF16Max, nraw = 0;
-  for (; nf16 >= 2; --nf16) {
-    const size_t fixed = (size_t)nf16 * p.f16_stage + scale_bytes + misc;
-    nraw = fixed < (size_t)optin ? (int)(((size_t)optin - fixed) / p.raw_stage) : 0;
+  // shared memory: two tile-scale buffers, the packed-weight ring, the
+  // operand (Bhi / Blo) ring, the token-row ring, small state.  Operand
+  // stages also take tensor memory (nm x 32 columns each, after the two
+  // accumulator buffers); packed-weight stages get what shared memory is left.
+  const uint32_t nb = (uint32_t)K / 32;
+  p.scale_buf = (uint32_t)nm * kTcRows * nb;
+  const int na_tmem = (int)((kTmemCols - kAccCols) / (32u * (uint32_t)nm));
+  const size_t fixed0 = 2u * (size_t)p.scale_buf + (size_t)kBAhead * kBRawSlot + tc_shared_bytes(E) + 1024u + 64u;
+  int nA = na_tmem < kMaxA ? na_tmem : kMaxA, nraw = 0;
+  const int min_a = 4 / nm + 1;
+  for (; nA >= min_a; --nA) {
+    const size_t fixed = fixed0 + (size_t)nA * kBStage;
+    nraw = fixed < (size_t)optin ? (int)(((size_t)optin - fixed) / ((size_t)nm * kRawMat)) : 0;
     if (nraw >= 3) break;
   }
-  if (nraw > kTcRawMax) nraw = kTcRawMax;
-  if (nf16 < 2 || nraw < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path does not fit shared memory", name);
-  p.nf16 = nf16;
+  if (nA < min_a) nA = min_a;
+  if (nraw > kMaxRaw) nraw = kMaxRaw;
+  if (nraw < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path does not fit shared memory", name);
+  p.nA = nA;
   p.nraw = nraw;
-  p.off_f16 = 0;
-  p.off_scale = (uint32_t)nf16 * p.f16_stage;
-  p.off_raw = p.off_scale + scale_bytes;
-  p.off_misc = p.off_raw + (uint32_t)nraw * p.raw_stage;
-  const size_t smem = p.off_misc + tc_misc_bytes(E);
+  p.off_scale = 0;
+  p.off_raw = 2u * p.scale_buf;  // a multiple of 1024 (swizzled copies land 1024-aligned)
+  p.off_b = p.off_raw + (uint32_t)nraw * nm * kRawMat;
+  p.off_braw = p.off_b + (uint32_t)nA * kBStage;
+  p.off_misc = (p.off_braw + (uint32_t)kBAhead * kBRawSlot + 63u) & ~63u;
+  const size_t smem = (size_t)p.off_misc + tc_shared_bytes(E) + 1024u;  // + alignment of the base
   if (smem > (size_t)optin) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs %zu bytes of shared memory", name, smem);
   auto kern = nm == 2 ? tc_expert_kernel<2> : tc_expert_kernel<1>;
   static bool configured[2][64] = {};
