@@ -66,6 +66,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="layer copies to cycle (default: per workload)")
+    ap.add_argument("--graph-steps", type=int, default=16, help="layer forwards captured per CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the cpu_baseline sample")
     return ap.parse_args()
 
@@ -278,32 +279,50 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize(dev)  # weights, inputs and workspace are written on the default stream
 
-    # ---- capture one graph per (layer, batch), gate/up bracketed by events
+    # ---- graphs.  Step s of the run uses pair s % NG = (layer copy, batch).
+    # Single-step graphs serve the routing pass and any remainder; the timed
+    # steps replay multi-step graphs of S consecutive steps, so the per-graph
+    # launch cost is paid once per S layer forwards (as in a model whose whole
+    # decode step is one graph).  Fused path: no events inside the timed
+    # graphs, its kernel time is the timed region over K launches.  Stage
+    # path: events bracket the gate/up kernel of the first step of each graph.
     try:
         mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
         mk_ev()
         in_graph_events = True
     except TypeError:
         in_graph_events = False
-    graphs, gu_events = [], []
     fused = moe.MoeLayer(layers[0]).use_fused(T)
     stage = "decode" if fused else "gateup"   # the dominant kernel
+    S = args.graph_steps if (args.graph_steps > 1 and NG % args.graph_steps == 0) else 1
+
+    def pair(s):
+        return layers[s % NG % NL], xs[(s % NG // NL) % NX]
+
+    singles, multis, multi_events = [], [], []
     with torch.cuda.stream(stream):
         for gi in range(NG):
-            lw, x = layers[gi % NL], xs[(gi // NL) % NX]
+            lw, x = pair(gi)
             layer = moe.MoeLayer(lw)
             layer.forward(x, ws, stream)  # warm / first-call set-up outside capture
-            ev = {stage: (mk_ev(), mk_ev())} if in_graph_events else None
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                layer.forward(x, ws, stream, events=ev)
-            graphs.append(g)
-            gu_events.append(ev)
+                layer.forward(x, ws, stream)
+            singles.append(g)
+        for gj in range(NG // S):
+            ev = {stage: (mk_ev(), mk_ev())} if (in_graph_events and not fused) else None
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(S):
+                    lw, x = pair(gj * S + i)
+                    moe.MoeLayer(lw).forward(x, ws, stream, events=ev if i == 0 else None)
+            multis.append(g)
+            multi_events.append(ev)
     torch.cuda.synchronize(dev)
 
-    # ---- routing of every graph (for algorithmic bytes)
+    # ---- routing of every step pair (for algorithmic bytes)
     uniq = []
-    for g in graphs:
+    for g in singles:
         g.replay()
         torch.cuda.synchronize(dev)
         uniq.append(int(torch.unique(ws.ids).numel()))
@@ -314,11 +333,19 @@ def main():
     else:
         gu_bytes = [u * 2 * I_EXP * (H // 2 + H // 32) + T * (H + H // 32 * 4) + A * I_EXP * 4 for u in uniq]
 
-    # ---- warm-up: W steps, plus enough to bring clocks up (~0.3 s)
     def run(n, start=0):
-        for s in range(start, start + n):
-            graphs[s % NG].replay()
+        """Steps start .. start+n-1: whole multi-step graphs where they line
+        up, single-step graphs for the rest."""
+        s, end = start, start + n
+        while s < end:
+            if s % S == 0 and end - s >= S:
+                multis[(s % NG) // S].replay()
+                s += S
+            else:
+                singles[s % NG].replay()
+                s += 1
 
+    # ---- warm-up: W steps, plus enough to bring clocks up (~0.3 s)
     with torch.cuda.stream(stream):
         run(max(3, args.warmup))
         t0 = time.perf_counter()
@@ -327,7 +354,7 @@ def main():
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
 
-    # ---- timed region
+    # ---- timed region: exactly K steps, starting at step 0 of the cycle
     K = args.steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -343,11 +370,19 @@ def main():
         if dist:
             dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    last = [(s % NG) for s in range(max(0, K - NG), K)]
-    if in_graph_events:
-        gu_ms = [gu_events[g][stage][0].elapsed_time(gu_events[g][stage][1]) for g in last]
+    if fused:
+        # one launch per step: the kernel's average duration over the timed
+        # region (launch gaps included, so an upper bound)
+        gu_steps = list(range(K))
+        gu_ms = [ms / K] * K
+    elif in_graph_events:
+        # the gate/up launches of the first step of the last multi-step graphs replayed
+        firsts = [s for s in range(0, K - K % S, S)][-len(multis):]
+        gu_steps = firsts
+        gu_ms = [multi_events[(s % NG) // S][stage][0].elapsed_time(multi_events[(s % NG) // S][stage][1])
+                 for s in firsts]
     else:
-        gu_ms = []
+        gu_steps, gu_ms = [], []
     if dist:
         t = torch.tensor([ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -402,7 +437,7 @@ def main():
     hbm_peak, peak_kind = peaks()
     roofline = None
     if gu_ms:
-        gb = sum(gu_bytes[g] for g in last)
+        gb = sum(gu_bytes[s % NG] for s in gu_steps)
         achieved = gb / (sum(gu_ms) * 1e-3) / 1e9
         roofline = {"kernel": "moe_decode_forward" if fused else "moe_mxfp4_gateup_swiglu", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
@@ -426,7 +461,7 @@ def main():
                        "activations": "bf16 N(0,1) -> Q8 per 32", "router": "bf16",
                        "zipf_bias": zipf, "parallelism": f"replicas{world}",
                        "l2": f"{NL} layer copies x {NX} token batches cycled ({NL * 3.42:.1f} GB of weights > L2)",
-                       "graph": "one CUDA graph per (layer copy, batch), replayed back to back",
+                       "graph": f"CUDA graphs of {S} consecutive layer forwards (distinct layer copies), replayed back to back",
                        "path": "fused single-launch decode" if fused else "six stage calls (8 kernels)",
                        "distinct_experts_mean": sum(uniq) / len(uniq)},
             "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,

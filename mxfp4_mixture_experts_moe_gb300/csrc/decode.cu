@@ -147,19 +147,6 @@ MOE_DEVFN bool wait_count(unsigned long long *ctr, unsigned long long target, un
   }
 }
 
-// 8 consecutive bf16 / fp32 values from shared memory, widened exactly.
-MOE_DEVFN void load8_smem(uint32_t addr, bool bf16, float (&v)[8]) {
-  if (bf16) {
-    const uint4 r = lds128(addr);
-    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
-    v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
-  } else {
-    const uint4 a = lds128(addr), b = lds128(addr + 16);
-    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
-    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-  }
-}
-
 MOE_DEVFN void load32_smem(uint32_t addr, bool bf16, float (&v)[32]) {
   const uint32_t step = bf16 ? 16u : 32u;
 #pragma unroll
@@ -172,7 +159,7 @@ MOE_DEVFN void load32_smem(uint32_t addr, bool bf16, float (&v)[32]) {
 }
 
 // One router logit (one expert row, one token) from shared memory, one warp,
-// in the order of router_logits_warp: lane l accumulates the chunks l, l+32,
+// in the order of the router kernels: lane l accumulates the chunks l, l+32,
 // ... of 8 consecutive inputs in increasing order with one fma per element,
 // then the 32 partial sums meet in an xor butterfly.  The chunk loads of four
 // consecutive passes are issued together; the fma order is unchanged.

@@ -40,62 +40,21 @@ MOE_DEVFN void sts32(uint32_t addr, uint32_t v) {
 MOE_DEVFN float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 MOE_DEVFN float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 8 consecutive inputs (bf16 or fp32) from global memory, widened exactly.
-MOE_DEVFN void load8(const void *base, bool bf16, int64_t elem, float (&v)[8]) {
+// ------------------------------------------------------------------ router
+
+// 8 consecutive bf16 / fp32 values from shared memory, widened exactly.
+MOE_DEVFN void load8_smem(uint32_t addr, bool bf16, float (&v)[8]) {
   if (bf16) {
-    const uint4 r = ldg_nc(static_cast<const uint16_t *>(base) + elem);
+    const uint4 r = lds128(addr);
     v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
     v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
   } else {
-    const float *p = static_cast<const float *>(base) + elem;
-    const uint4 a = ldg_nc(p), b = ldg_nc(p + 4);
+    const uint4 a = lds128(addr), b = lds128(addr + 16);
     v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
     v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
   }
 }
 
-// ------------------------------------------------------------------ router
-
-// Router logit of one expert for up to 8 tokens, one warp.  Lane l owns the
-// chunks l, l+32, ... of 8 consecutive inputs and accumulates them in
-// increasing order with one fma per element; the 32 partial sums are added by
-// an xor butterfly, whose lane-0 value is ((p0+p16)+(p8+p24))+... .  The
-// router row is read 8 chunks per lane at a time (all loads in flight
-// together); the order of the fmas is unchanged by that batching.
-template <int NB = 8>
-MOE_DEVFN void router_logits_warp(const void *x, bool xbf, int64_t ld_x, const void *wr, bool wbf, int e, int t0,
-                                  int nt, int H, float (&p)[8]) {
-  const int lane = threadIdx.x & 31;
-  const int nch = H / 8;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) p[j] = 0.0f;
-  for (int c0 = lane; c0 < nch; c0 += 32 * NB) {
-    float wv[NB][8];
-#pragma unroll
-    for (int i = 0; i < NB; ++i)
-      if (c0 + 32 * i < nch) load8(wr, wbf, (int64_t)e * H + 8 * (c0 + 32 * i), wv[i]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < nt) {
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const int c = c0 + 32 * i;
-          if (c < nch) {
-            float xv[8];
-            load8(x, xbf, (int64_t)(t0 + j) * ld_x + 8 * c, xv);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) p[j] = __fmaf_rn(xv[q], wv[i][q], p[j]);
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], s));
-  }
-}
 
 // Top-k of one token, one warp.  score = logit (+ bias); the k largest
 // scores are taken in descending order, equal scores by lower expert id, and

@@ -9,23 +9,136 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 4;   // warps per CTA, one expert each
-constexpr int kRouteTokens = 8;  // tokens per warp pass (register tile)
+constexpr int kRouteWarps = 4;   // warps per CTA, each on its own EW experts
+constexpr int kRouteTokens = 8;  // tokens per CTA (register tile)
+constexpr int kRouteSlab = 64;   // 8-element chunks per shared-memory slab (512 inputs)
 
-// logits[t, e] for one expert per warp and kRouteTokens tokens per CTA row.
+// logits[t, e] for a tile of kRouteWarps*EW experts x kRouteTokens tokens.
+// The tile's router rows and activation rows pass through shared memory in
+// slabs of 512 inputs (cp.async, double-buffered), so each input is read
+// from L2 once per tile instead of once per (expert, token).  Every logit
+// keeps the fixed order of the layer's router: lane l accumulates the
+// 8-element chunks l, l+32, l+64, ... in increasing order, one fma per
+// element, then the 32 partial sums meet in an xor butterfly (whose value is
+// the same in every lane, IEEE addition being commutative).  So the bits of
+// a logit depend neither on T nor on the tile it falls in.
+template <int EW, bool XBF, bool WBF>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-route_logits_kernel(const void *x, bool xbf, int64_t ld_x, const void *wr, bool wbf, int T, int H, int E,
-                    float *logits) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  const int t0 = blockIdx.y * kRouteTokens;
-  if (e >= E) return;
-  const int nt = min(kRouteTokens, T - t0);
-  float p[8];
-  router_logits_warp(x, xbf, ld_x, wr, wbf, e, t0, nt, H, p);
+route_logits_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  constexpr uint32_t xsz = XBF ? 2 : 4, wsz = WBF ? 2 : 4;
+  constexpr uint32_t wrow = kRouteSlab * 8 * wsz, xrow = kRouteSlab * 8 * xsz;  // bytes per row and slab
+  constexpr int nw = kRouteWarps * EW;                                            // router rows per tile
+  constexpr uint32_t wbytes = nw * wrow, slab_bytes = wbytes + kRouteTokens * xrow;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e0 = blockIdx.x * nw, t0 = blockIdx.y * kRouteTokens;
+  const int nch = H / 8, nslab = (nch + kRouteSlab - 1) / kRouteSlab;
+  const uint32_t base = smem_addr(rsm);
+
+  // rows past E or T are read from the last valid row; their sums are never stored
+  auto stage = [&](int sl, int buf) {
+    const uint32_t dst = base + (uint32_t)buf * slab_bytes;
+    const int elem0 = sl * kRouteSlab * 8;
+    constexpr int wp = wrow / 16, xp = xrow / 16;
+    for (int i = tid; i < nw * wp; i += kRouteWarps * 32) {
+      const int r = i / wp, q = i - r * wp;
+      const int elem = elem0 + q * (16 / wsz);
+      if (elem < H)
+        cp_async16(dst + r * wrow + q * 16,
+                   static_cast<const uint8_t *>(wr) + ((int64_t)min(e0 + r, E - 1) * H + elem) * wsz);
+    }
+    for (int i = tid; i < kRouteTokens * xp; i += kRouteWarps * 32) {
+      const int r = i / xp, q = i - r * xp;
+      const int elem = elem0 + q * (16 / xsz);
+      if (elem < H)
+        cp_async16(dst + wbytes + r * xrow + q * 16,
+                   static_cast<const uint8_t *>(x) + ((int64_t)min(t0 + r, T - 1) * ld_x + elem) * xsz);
+    }
+    cp_async_commit();
+  };
+
+  float p[EW][kRouteTokens];
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (lane == 0 && j < nt) logits[(int64_t)(t0 + j) * E + e] = p[j];
+  for (int i = 0; i < EW; ++i)
+#pragma unroll
+    for (int j = 0; j < kRouteTokens; ++j) p[i][j] = 0.0f;
+  stage(0, 0);
+#pragma unroll 1
+  for (int sl = 0; sl < nslab; ++sl) {
+    if (sl + 1 < nslab) {
+      stage(sl + 1, (sl + 1) & 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t sb = base + (uint32_t)(sl & 1) * slab_bytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cl = lane + 32 * h;  // chunk within the slab
+      if (sl * kRouteSlab + cl < nch) {
+        float wv[EW][8];
+#pragma unroll
+        for (int i = 0; i < EW; ++i) load8_smem(sb + (uint32_t)(warp * EW + i) * wrow + (uint32_t)cl * 8 * wsz, WBF, wv[i]);
+#pragma unroll
+        for (int j = 0; j < kRouteTokens; ++j) {
+          float xv[8];
+          load8_smem(sb + wbytes + (uint32_t)j * xrow + (uint32_t)cl * 8 * xsz, XBF, xv);
+#pragma unroll
+          for (int i = 0; i < EW; ++i)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) p[i][j] = __fmaf_rn(xv[q], wv[i][q], p[i][j]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < EW; ++i)
+#pragma unroll
+    for (int j = 0; j < kRouteTokens; ++j)
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) p[i][j] = __fadd_rn(p[i][j], __shfl_xor_sync(0xffffffffu, p[i][j], s));
+#pragma unroll
+  for (int i = 0; i < EW; ++i) {
+#pragma unroll
+    for (int j = 0; j < kRouteTokens; ++j) {
+      const int e = e0 + warp * EW + i, t = t0 + j;
+      if (lane == i * kRouteTokens + j && e < E && t < T) logits[(int64_t)t * E + e] = p[i][j];
+    }
+  }
+}
+
+template <int EW, bool XBF, bool WBF>
+cudaError_t launch_route_logits(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits,
+                                cudaStream_t s) {
+  constexpr uint32_t smem = 2u * (kRouteWarps * EW * kRouteSlab * 8 * (WBF ? 2 : 4) +
+                                  kRouteTokens * kRouteSlab * 8 * (XBF ? 2 : 4));
+  static_assert(smem <= 227 * 1024, "slabs fit shared memory");
+  if (smem > 48 * 1024) {
+    static bool done[64] = {};  // per device; setting it twice (racing threads) is harmless
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(route_logits_kernel<EW, XBF, WBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) done[dev] = true;
+    }
+  }
+  dim3 grid((E + kRouteWarps * EW - 1) / (kRouteWarps * EW), (T + kRouteTokens - 1) / kRouteTokens);
+  route_logits_kernel<EW, XBF, WBF><<<grid, kRouteWarps * 32, smem, s>>>(x, ld_x, wr, T, H, E, logits);
+  return cudaGetLastError();
+}
+
+template <int EW>
+cudaError_t launch_route_logits_dt(bool xbf, bool wbf, const void *x, int64_t ld_x, const void *wr, int T, int H,
+                                   int E, float *logits, cudaStream_t s) {
+  if (xbf && wbf) return launch_route_logits<EW, true, true>(x, ld_x, wr, T, H, E, logits, s);
+  if (xbf) return launch_route_logits<EW, true, false>(x, ld_x, wr, T, H, E, logits, s);
+  if (wbf) return launch_route_logits<EW, false, true>(x, ld_x, wr, T, H, E, logits, s);
+  return launch_route_logits<EW, false, false>(x, ld_x, wr, T, H, E, logits, s);
 }
 
 // Top-k per token, one warp per token.
@@ -68,11 +181,12 @@ extern "C" moe_status moe_route_topk(const void *x, moe_dtype x_dtype, int64_t l
   if (ld_x < H || (ld_x * xes) % 16) return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: ld_x=%lld", (long long)ld_x);
   if ((uintptr_t)x % 16 || (uintptr_t)w_router % 16) return fail(MOE_ERR_INVALID_ARG, "moe_route_topk: x and w_router must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid((E + kRouteWarps - 1) / kRouteWarps, (T + kRouteTokens - 1) / kRouteTokens);
-  if (grid.y > 65535) return fail(MOE_ERR_UNSUPPORTED, "moe_route_topk: T=%d too large", T);
-  route_logits_kernel<<<grid, kRouteWarps * 32, 0, s>>>(x, x_dtype == MOE_BF16, ld_x, w_router, w_dtype == MOE_BF16,
-                                                        T, H, E, logits);
-  cudaError_t err = cudaGetLastError();
+  if ((T + kRouteTokens - 1) / kRouteTokens > 65535) return fail(MOE_ERR_UNSUPPORTED, "moe_route_topk: T=%d too large", T);
+  // experts per warp: more CTAs for small batches, more reuse of each staged input for large ones
+  const bool xbf = x_dtype == MOE_BF16, wbf = w_dtype == MOE_BF16;
+  cudaError_t err = T <= 8    ? launch_route_logits_dt<1>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
+                    : T <= 64 ? launch_route_logits_dt<2>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
+                              : launch_route_logits_dt<4>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_route_topk: logits launch");
   topk_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, bias, T, E, k, ids, weights);
   err = cudaGetLastError();

@@ -30,7 +30,8 @@ def _spec(name):
 # ----------------------------------------------------------------- router
 
 @pytest.mark.parametrize("name,T,pad", [("tiny", 1, 0), ("tiny", 7, 24), ("dsv4", 1, 0), ("dsv4", 16, 8),
-                                        ("dsv4", 37, 0), ("zipf", 64, 0), ("odd", 9, 40)])
+                                        ("dsv4", 37, 0), ("zipf", 64, 0), ("odd", 9, 40), ("dsv4", 130, 0),
+                                        ("tiny", 77, 16), ("odd", 66, 8)])
 def test_route_topk(moe, name, T, pad):
     spec = _spec(name)
     x = synth.activations(spec, T, token0=3)
