@@ -59,9 +59,11 @@ struct DecodeArgs {
   int nstage;
   uint32_t stage_bytes;
   uint32_t gwreg, gsreg;  // gate/up stage: weight / scale region per matrix
-  uint32_t dwreg;         // down stage: weight region
+  uint32_t dwreg;         // down slice: weight region (scale bytes follow)
+  uint32_t dslot;         // bytes of one down slice in a stage (128-aligned)
+  int dpp;                // down slices per ring stage
   uint32_t xrow, hrow;    // staged activation row bytes
-  uint32_t off_bars, off_act, off_hbuf, off_y, off_logit, off_misc;
+  uint32_t off_bars, off_act, off_hq, off_y, off_logit, off_misc;
   int Rd;                 // max down rows per CTA (row stride of the y slice)
   int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
   int g16, d16;           // scale bytes copyable in 16-byte pieces
@@ -383,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     }
     mbar_init(smem_addr(fbar), 1);
     fence_mbar_init();
+    m.scalars[4] = 0;
     // stage this CTA's router rows and the T activation rows with bulk copies
     int nrows = 0;
     for (int w = 0; w < nrw; ++w) nrows += (cta + G * w) < E;
@@ -469,13 +472,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const int n0g = (int)((unsigned)(cta * I) / (unsigned)G), Rg = (int)((unsigned)((cta + 1) * I) / (unsigned)G) - n0g;
   const int n0d = (int)((unsigned)(cta * H) / (unsigned)G), Rd = (int)((unsigned)((cta + 1) * H) / (unsigned)G) - n0d;
 
+  const int ndi = (nact + p.dpp - 1) / p.dpp;  // down ring items (dpp slots each)
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
+    // streams this CTA's gate/up slice of every active expert through the
+    // ring, then its down slices, dpp slots per stage; once the first stages
+    // are requested it asks for the down slices to be pulled into L2, so the
+    // down copies (issued when gate/up stages free up) read from L2
     const uint64_t pol = policy_evict_first();
     const uint32_t gw = (uint32_t)Rg * (H / 2), gs = (uint32_t)Rg * nbH;
     const uint32_t dw = (uint32_t)Rd * (I / 2), ds = (uint32_t)Rd * nbI;
+    const int first = nact < nstage ? nact : nstage;
     int issued = 0;
-    for (int it = 0; it < 2 * nact; ++it) {
+    for (int it = 0; it < nact + ndi; ++it) {
       const int st = it % nstage;
       if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
       const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
@@ -502,29 +511,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
           }
         }
       } else {
-        const int64_t row0 = (int64_t)m.active[it - nact] * H + n0d;
+        const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, dw + (p.d16 ? ds : 0u));
+          mbar_arrive_expect_tx(fb, (uint32_t)(j1 - j0) * (dw + (p.d16 ? ds : 0u)));
           if (dw > 0) {
-            bulk_g2s(sbase, p.wd + row0 * (I / 2), dw, fb, pol);
-            if (p.d16) bulk_g2s(sbase + p.dwreg, p.sd + row0 * nbI, ds, fb, pol);
+            for (int j = j0; j < j1; ++j) {
+              const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
+              const uint32_t dst = sbase + (uint32_t)(j - j0) * p.dslot;
+              bulk_g2s(dst, p.wd + drow0 * (I / 2), dw, fb, pol);
+              if (p.d16) bulk_g2s(dst + p.dwreg, p.sd + drow0 * nbI, ds, fb, pol);
+            }
           }
         }
         if (!p.d16) {
-          const uint8_t *src = p.sd + row0 * nbI;
-          const uint32_t dst = sbase + p.dwreg;
-          for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+          for (int j = j0; j < j1; ++j) {
+            const uint8_t *src = p.sd + ((int64_t)m.active[j] * H + n0d) * nbI;
+            const uint32_t dst = sbase + (uint32_t)(j - j0) * p.dslot + p.dwreg;
+            for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+          }
         }
       }
       cp_async_mbar_arrive_noinc(fb);
       issued = it + 1;
-      // once every gate/up slice is requested, pull this CTA's down slices
-      // into L2 so that the down half of the ring reads from L2
-      if (it == nact - 1 && dw > 0) {
+      if (it == first - 1 && dw > 0) {
         for (int j = lane; j < nact; j += 32) {
-          const int64_t row0 = (int64_t)m.active[j] * H + n0d;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + row0 * (I / 2)), "r"(dw) : "memory");
-          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + row0 * nbI), "r"(ds) : "memory");
+          const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + drow0 * (I / 2)), "r"(dw) : "memory");
+          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + drow0 * nbI), "r"(ds) : "memory");
         }
       }
     }
@@ -534,54 +547,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   }
 
   // -------------------------------------------------------------- consumers
-  // Two groups of kGroup warps take alternate ring items (group g: items g,
-  // g+2, ...), so two items are computed at once.  A gate/up unit is one
+  // Gate/up: two groups of kGroup warps take alternate ring items (group g:
+  // items g, g+2, ...), so two items are computed at once.  A unit is one
   // output row of the expert, both matrices in one warp, SwiGLU in the warp;
   // when a group has written its h slice of expert slot j it counts that in
-  // the workspace word of slot j.  A down item for slot j waits until all
-  // CTAs have counted, quantises that expert's h rows into the group's own
-  // buffer, then computes units of two down rows sharing the activation loads.
-  // A warp whose wait gave up stops computing but keeps arriving on the ring
-  // and on the named barriers, so no other warp is left waiting on it.
+  // the workspace word of slot j.
+  // Down: once every slot is counted by all CTAs, all consumer warps
+  // quantise every h row into the (now idle) ring area at once, then take
+  // units of two down rows of one slot, reading the weights from L2 (the
+  // producer prefetched them there), and leave y in shared memory for the
+  // combine.  A warp whose wait gave up stops computing but keeps arriving
+  // on the ring and on the named barriers, so no other warp waits on it.
   const int grp = warp / kGroup, gw = warp - grp * kGroup;
   const int gbar = 3 + grp;  // named barrier of this group
-  const uint32_t hbuf = smem_addr(smem + p.off_hbuf) + (uint32_t)grp * (uint32_t)T * p.hrow;
   bool dead = false;
-  for (int it = grp; it < 2 * nact; it += 2) {
+  for (int it = grp; it < nact; it += 2) {
     const int st = it % nstage;
-    const int j = it - nact;  // expert slot of a down item
-    if (j >= 0) {
-      if (gw == 0 && lane == 0)
-        m.scalars[2 + grp] = !dead && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
-      bar_sync_named(gbar, kGroup * 32);
-      dead = dead || m.scalars[2 + grp] == 0;
-      if (!dead) {
-        const int sb = m.segb[j], nrow = m.segb[j + 1] - sb;
-        for (int idx0 = gw * 32; idx0 < 2 * nrow * nbI; idx0 += kGroup * 32) {
-          const int idx = idx0 + lane;  // 2 * block + half
-          const bool valid = idx < 2 * nrow * nbI;
-          const int blk = valid ? idx >> 1 : 0, half = idx & 1;
-          const int ql = blk / nbI, b = blk - ql * nbI;
-          float v[16];
-          const float *src = p.h + (int64_t)m.srt[sb + ql] * p.ld_h + 32 * b + 16 * half;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 r = valid ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
-            v[4 * c] = __uint_as_float(r.x);
-            v[4 * c + 1] = __uint_as_float(r.y);
-            v[4 * c + 2] = __uint_as_float(r.z);
-            v[4 * c + 3] = __uint_as_float(r.w);
-          }
-          q8_pair_to_row(v, half, valid, hbuf + (uint32_t)ql * p.hrow, I, b);
-        }
-      }
-      bar_sync_named(gbar, kGroup * 32);
-    }
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
-    if (dead) {
-      // skip the work
-    } else if (j < 0) {
+    if (!dead) {
       const int sb = m.segb[it], se = m.segb[it + 1];
 #pragma unroll 1
       for (int r = gw; r < Rg; r += kGroup) {
@@ -599,37 +583,93 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
           if (lane == 0) p.h[(int64_t)a * p.ld_h + n0g + r] = __fmul_rn(silu(g), u);
         }
       }
-    } else {
-      const int sb = m.segb[j], se = m.segb[j + 1];
+    }
+    // this CTA's h slice of expert slot it is written: count it (release)
+    bar_sync_named(gbar, kGroup * 32);
+    if (gw == 0 && lane == 0)
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSlotWord + it), "l"(1ull) : "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+  }
+
+  // ---- down phase
+  if (dead && lane == 0) m.scalars[4] = 1;
+  bar_sync_named(1, kCons * 32);
+  if (warp == 0) {
+    bool ok = m.scalars[4] == 0;
+    for (int j = lane; j < nact; j += 32) ok = ok && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) m.scalars[5] = ok;
+  }
+  bar_sync_named(1, kCons * 32);
+  const bool hdead = m.scalars[5] == 0;
+  const uint32_t hq = smem_addr(smem + p.off_hq);  // Q8(h) rows by sorted position
+  const int nq = m.segb[nact];
+  if (!hdead) {
+    // Q8 of every h row, two blocks per lane pair and pass (loads first)
+    const int ntask = 2 * nq * nbI;  // (row, block, half)
+    for (int idx0 = warp * 64; idx0 < ntask; idx0 += kCons * 64) {
+      float v[2][16];
+      bool valid[2];
+      int ql[2], b[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = idx0 + 32 * u + lane;
+        valid[u] = idx < ntask;
+        const int blk = valid[u] ? idx >> 1 : 0;
+        ql[u] = blk / nbI;
+        b[u] = blk - ql[u] * nbI;
+        const float *src = p.h + (int64_t)m.srt[ql[u]] * p.ld_h + 32 * b[u] + 16 * (idx & 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 r = valid[u] ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
+          v[u][4 * c] = __uint_as_float(r.x);
+          v[u][4 * c + 1] = __uint_as_float(r.y);
+          v[u][4 * c + 2] = __uint_as_float(r.z);
+          v[u][4 * c + 3] = __uint_as_float(r.w);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) q8_pair_to_row(v[u], lane & 1, valid[u], hq + (uint32_t)ql[u] * p.hrow, I, b[u]);
+    }
+  }
+  bar_sync_named(1, kCons * 32);
+  dead = dead || hdead;
+  // down ring items: the groups keep alternating items (item it, slots
+  // (it - nact) * dpp ...); a unit is two rows of one slot sharing the
+  // activation loads
+  for (int it = nact + ((grp - nact) % 2 + 2) % 2; it < nact + ndi; it += 2) {
+    const int st = it % nstage;
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
+    if (!dead) {
+      const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
+      for (int j = j0; j < j1; ++j) {
+        const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes) + (uint32_t)(j - j0) * p.dslot;
+        const int sb = m.segb[j], se = m.segb[j + 1];
 #pragma unroll 1
-      for (int r = gw; r < Rd; r += 2 * kGroup) {
-        const bool two = r + kGroup < Rd;
-        const int r2 = two ? r + kGroup : r;  // one row left: both halves read row r
-        const uint32_t wrow[2] = {sbase + (uint32_t)r * (I / 2), sbase + (uint32_t)r2 * (I / 2)};
-        const uint32_t srow[2] = {sbase + p.dwreg + (uint32_t)r * nbI, sbase + p.dwreg + (uint32_t)r2 * nbI};
+        for (int r = gw; r < Rd; r += 2 * kGroup) {
+          const bool two = r + kGroup < Rd;
+          const int r2 = two ? r + kGroup : r;  // one row left: both halves read row r
+          const uint32_t wrow[2] = {sbase + (uint32_t)r * (I / 2), sbase + (uint32_t)r2 * (I / 2)};
+          const uint32_t srow[2] = {sbase + p.dwreg + (uint32_t)r * nbI, sbase + p.dwreg + (uint32_t)r2 * nbI};
 #pragma unroll 1
-        for (int q = sb; q < se; ++q) {
-          const int a = m.srt[q];
-          float acc[2];
-          row_dot_stage_pn<2, SD>(hbuf + (uint32_t)(q - sb) * p.hrow, I, wrow, srow, acc);
-          float v0, v1;
-          reduce_pair(acc[0], acc[1], v0, v1);
-          if (lane == 0) {
-            yslice[a * p.Rd + r] = v0;
-            if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v0;
-            if (two) {
-              yslice[a * p.Rd + r + kGroup] = v1;
-              if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r + kGroup] = v1;
+          for (int q = sb; q < se; ++q) {
+            const int a = m.srt[q];
+            float acc[2];
+            row_dot_stage_pn<2, SD>(hq + (uint32_t)q * p.hrow, I, wrow, srow, acc);
+            float v0, v1;
+            reduce_pair(acc[0], acc[1], v0, v1);
+            if (lane == 0) {
+              yslice[a * p.Rd + r] = v0;
+              if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v0;
+              if (two) {
+                yslice[a * p.Rd + r2] = v1;
+                if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r2] = v1;
+              }
             }
           }
         }
       }
-    }
-    if (j < 0) {
-      // this CTA's h slice of expert slot it is written: count it (release)
-      bar_sync_named(gbar, kGroup * 32);
-      if (gw == 0 && lane == 0)
-        asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSlotWord + it), "l"(1ull) : "memory");
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
@@ -680,15 +720,19 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.gsreg = align16((uint64_t)Rg * nbH);
   p.dwreg = (uint32_t)Rd * (I / 2);
   const uint32_t gstage = 2 * (p.gwreg + p.gsreg), dstage = p.dwreg + align16((uint64_t)Rd * nbI);
-  p.stage_bytes = ((gstage > dstage ? gstage : dstage) + 127u) & ~127u;
+  p.dslot = (dstage + 127u) & ~127u;
+  p.stage_bytes = ((gstage > p.dslot ? gstage : p.dslot) + 127u) & ~127u;
+  p.dpp = (int)(p.stage_bytes / p.dslot);
   p.xrow = (uint32_t)H + 8u * nbH;
   p.hrow = (uint32_t)I + 8u * nbI;
   const uint64_t act_bytes = align16((uint64_t)T * p.xrow);
-  const uint64_t hbuf_bytes = align16(2ull * T * p.hrow);  // one T-row buffer per consumer group
+  // Q8(h) of every assignment, in the region of Q8(x): the down phase
+  // starts after every gate/up unit has read its activations
+  const uint64_t hq_bytes = align16((uint64_t)A * p.hrow);
   const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
-  const uint64_t misc_bytes = align16(4ull * (7 * A + 5));  // ids w srt skey segb active + 4 scalars
-  const uint64_t tail = 16ull * 8 + act_bytes + hbuf_bytes + y_bytes + logit_bytes + misc_bytes;
+  const uint64_t misc_bytes = align16(4ull * (6 * A + 1 + 8));  // ids w srt skey segb active + 8 scalars
+  const uint64_t tail = 16ull * 8 + std::max(act_bytes, hq_bytes) + y_bytes + logit_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   if (tail >= budget) return false;
   int ns = (int)((budget - tail) / p.stage_bytes);
@@ -701,8 +745,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   if (ring + tail > budget) return false;
   p.off_bars = (uint32_t)ring;
   p.off_act = p.off_bars + 16 * 8;
-  p.off_hbuf = p.off_act + (uint32_t)act_bytes;
-  p.off_y = p.off_hbuf + (uint32_t)hbuf_bytes;
+  p.off_hq = p.off_act;
+  p.off_y = p.off_act + (uint32_t)std::max(act_bytes, hq_bytes);
   p.off_logit = p.off_y + (uint32_t)y_bytes;
   p.off_misc = p.off_logit + (uint32_t)logit_bytes;
   *smem_out = p.off_misc + misc_bytes;
