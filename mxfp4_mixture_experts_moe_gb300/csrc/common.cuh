@@ -19,15 +19,15 @@ moe_status cuda_fail(cudaError_t e, const char *what);
 unsigned *device_status_word();  // per-device address of the status word, or NULL
 int sm_count();
 
-// Tensor-core path of the expert projections (tc_expert.cu): nm = 2 gate/up
-// with SwiGLU into out, nm = 1 down into out.  Used by the stage calls for
-// batches of more than kTensorMinRows - 1 rows.
+// Tensor-core path of the expert projections (tc_expert.cu): mode 0 gate/up
+// with SwiGLU into out0, 1 gate into out0 and up into out1, 2 down into out0.
+// Used by the stage calls for batches of more than kTensorMinRows - 1 rows.
 constexpr int kTensorMinRows = 17;
 bool tc_expert_supported(int K, int N);
-moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
+moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
                             const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
                             const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
-                            int K, int N, int bytoken, float *out, int64_t ld_out, cudaStream_t stream,
+                            int K, int N, int bytoken, float *out0, float *out1, int64_t ld_out, cudaStream_t stream,
                             const char *name);
 
 // Token of assignment a = t*k + j, i.e. a / k, as a multiply-high by

@@ -63,7 +63,7 @@ struct DecodeArgs {
   uint32_t dslot;         // bytes of one down slice in a stage (128-aligned)
   int dpp;                // down slices per ring stage
   uint32_t xrow, hrow;    // staged activation row bytes
-  uint32_t off_bars, off_act, off_hq, off_y, off_logit, off_misc;
+  uint32_t off_bars, off_act, off_hq, off_y, off_logit, off_cand, off_misc;
   int Rd;                 // max down rows per CTA (row stride of the y slice)
   int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
   int g16, d16;           // scale bytes copyable in 16-byte pieces
@@ -365,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const int E = p.E, k = p.k, T = p.T, A = p.A;
   const int nbH = H / 32, nbI = I / 32;
   const int nstage = p.nstage;
+  // this CTA's output slices (G * 4096 fits 32 bits)
+  const int n0g = (int)((unsigned)(cta * I) / (unsigned)G), Rg = (int)((unsigned)((cta + 1) * I) / (unsigned)G) - n0g;
+  const int n0d = (int)((unsigned)(cta * H) / (unsigned)G), Rd = (int)((unsigned)((cta + 1) * H) / (unsigned)G) - n0d;
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bars);
   uint64_t *empty = full + nstage;
@@ -443,10 +446,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // ---------------------------------------------------------------- A'
   for (int i = tid; i < T * E; i += kThreads) logit_s[i] = ldcg_f32(p.logits + i);
   __syncthreads();
+  // top-k in two stages: a warp per (token, group of 32 experts), then a
+  // warp per token merges the groups' candidates
+  const int ngrp = (E + 31) >> 5;  // <= 8 on this path
+  uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem + p.off_cand);
+  int *cand_id = reinterpret_cast<int *>(smem + p.off_cand) + T * 8 * 8;
+  for (int u = warp; u < T * ngrp; u += kWarps) {
+    const int t = u / ngrp, g = u - t * ngrp;
+    topk_group_stage(logit_s + t * E, p.bias, E, k, g, cand_key + u * k, cand_id + u * k);
+  }
+  __syncthreads();
   if (warp < T) {
     int id[8];
     float wv[8];
-    topk_warp_sorted<8>(logit_s + warp * E, p.bias, E, k, id, wv);  // E <= 256 on this path
+    topk_merge_stage(cand_key + warp * ngrp * k, cand_id + warp * ngrp * k, ngrp * k, k, id, wv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k && lane == j) {
@@ -468,11 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
   }
   const int nact = m.scalars[0];
-  // this CTA's output slices (G * 4096 fits 32 bits)
-  const int n0g = (int)((unsigned)(cta * I) / (unsigned)G), Rg = (int)((unsigned)((cta + 1) * I) / (unsigned)G) - n0g;
-  const int n0d = (int)((unsigned)(cta * H) / (unsigned)G), Rd = (int)((unsigned)((cta + 1) * H) / (unsigned)G) - n0d;
-
-  const int ndi = (nact + p.dpp - 1) / p.dpp;  // down ring items (dpp slots each)
+  const int ndi = p.dpp == 2 ? (nact + 1) >> 1 : (nact + p.dpp - 1) / p.dpp;  // down ring items (dpp slots each)
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
     // streams this CTA's gate/up slice of every active expert through the
@@ -731,8 +740,9 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t hq_bytes = align16((uint64_t)A * p.hrow);
   const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
+  const uint64_t cand_bytes = (uint64_t)T * 8 * 8 * 8;  // top-k candidates: T x 8 groups x 8 (key, id)
   const uint64_t misc_bytes = align16(4ull * (6 * A + 1 + 8));  // ids w srt skey segb active + 8 scalars
-  const uint64_t tail = 16ull * 8 + std::max(act_bytes, hq_bytes) + y_bytes + logit_bytes + misc_bytes;
+  const uint64_t tail = 16ull * 8 + std::max(act_bytes, hq_bytes) + y_bytes + logit_bytes + cand_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   if (tail >= budget) return false;
   int ns = (int)((budget - tail) / p.stage_bytes);
@@ -748,7 +758,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.off_hq = p.off_act;
   p.off_y = p.off_act + (uint32_t)std::max(act_bytes, hq_bytes);
   p.off_logit = p.off_y + (uint32_t)y_bytes;
-  p.off_misc = p.off_logit + (uint32_t)logit_bytes;
+  p.off_cand = p.off_logit + (uint32_t)logit_bytes;
+  p.off_misc = p.off_cand + (uint32_t)cand_bytes;
   *smem_out = p.off_misc + misc_bytes;
   return true;
 }

@@ -198,6 +198,70 @@ MOE_DEVFN void topk_warp_sorted(const float *logits_row, const float *bias, int 
   }
 }
 
+// Top-k in two stages for latency: stage 1, one warp per 32 consecutive
+// experts, takes that group's k best (score desc, id asc) by k rounds of warp
+// max; stage 2, one warp per token, merges the groups' lists the same way.
+// The selection order, the ids (0x7fffffff for a slot only NaN scores were
+// left for) and the weights are those of topk_warp_sorted: the best entry of
+// the union is the best entry of the group that holds it.
+// Stage 1 of expert group g (32 g .. 32 g + 31) of one token: writes k
+// (key, id) pairs to ck/ci.
+MOE_DEVFN void topk_group_stage(const float *logits_row, const float *bias, int E, int k, int g, uint32_t *ck,
+                                int *ci) {
+  const int lane = threadIdx.x & 31;
+  const int e = 32 * g + lane;
+  uint32_t key = e < E ? score_key(topk_score(logits_row, bias, e)) : 0u;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const int wl = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;  // lowest id holding it
+    if (lane == 0) {
+      ck[j] = kmax;
+      ci[j] = kmax ? 32 * g + wl : 0x7fffffff;
+    }
+    if (lane == wl) key = 0u;
+  }
+}
+
+// Stage 2: merge of n <= 64 (key, id) pairs into the k slots and weights
+// (every lane returns them).
+MOE_DEVFN void topk_merge_stage(const uint32_t *ck, const int *ci, int n, int k, int (&ids)[8], float (&w)[8]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ka = lane < n ? ck[lane] : 0u, kb = lane + 32 < n ? ck[lane + 32] : 0u;
+  int ia = lane < n ? ci[lane] : 0x7fffffff, ib = lane + 32 < n ? ci[lane + 32] : 0x7fffffff;
+  int my_id = 0;
+  float my_sel = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const bool a_first = ka > kb || (ka == kb && ia < ib);
+    const uint32_t bk = a_first ? ka : kb;
+    const int bi = a_first ? ia : ib;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const int win = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)bi : 0xffffffffu);
+    if (ka == kmax && ia == win) {
+      ka = 0u;
+      ia = 0x7fffffff;
+    } else if (kb == kmax && ib == win) {
+      kb = 0u;
+      ib = 0x7fffffff;
+    }
+    if (lane == j) {
+      my_id = kmax ? win : 0x7fffffff;
+      my_sel = kmax ? key_score(kmax) : -CUDART_INF_F;
+    }
+  }
+  const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-my_sel)));
+  float total = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) total = __fadd_rn(total, __shfl_sync(0xffffffffu, sg, j));
+  const float my_w = __fdiv_rn(sg, total);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ids[j] = j < k ? __shfl_sync(0xffffffffu, my_id, j) : 0;
+    w[j] = j < k ? __shfl_sync(0xffffffffu, my_w, j) : 0.0f;
+  }
+}
+
 MOE_DEVFN void topk_warp(const float *logits_row, const float *bias, int E, int k, int (&ids)[8], float (&w)[8]) {
   if (E <= 64) topk_warp_sorted<2>(logits_row, bias, E, k, ids, w);
   else if (E <= 256) topk_warp_sorted<8>(logits_row, bias, E, k, ids, w);

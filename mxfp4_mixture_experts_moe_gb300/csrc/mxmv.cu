@@ -327,9 +327,9 @@ static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const f
   if (ld < I) return fail(MOE_ERR_INVALID_ARG, "%s: output ld=%lld < I=%d", name, (long long)ld, I);
   if (mode == kGateUpRaw && (!o1 || (uintptr_t)o1 % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: bad up output", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mode == kGateUpSwiglu && T >= kTensorMinRows && tc_expert_supported(H, I))
-    return launch_tc_expert(2, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T * k, k, E, H, I, 1, o0,
-                            ld, s, name);
+  if (T >= kTensorMinRows && tc_expert_supported(H, I))
+    return launch_tc_expert(mode == kGateUpSwiglu ? 0 : 1, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap,
+                            T * k, k, E, H, I, 1, o0, mode == kGateUpSwiglu ? nullptr : o1, ld, s, name);
   MxArgs p{};
   p.aq = xq; p.ld_aq = ld_xq; p.as = xs; p.ld_as = ld_xs;
   p.w0 = wg; p.s0 = sg; p.w1 = wu; p.s1 = su;
@@ -369,8 +369,8 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
   if (st != MOE_OK || T == 0) return st;
   if (ld_y < H) return fail(MOE_ERR_INVALID_ARG, "%s: ld_y=%lld < H=%d", name, (long long)ld_y, H);
   if (T >= kTensorMinRows && tc_expert_supported(I, H))
-    return launch_tc_expert(1, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T * k, k, E, I,
-                            H, 0, y, ld_y, static_cast<cudaStream_t>(stream), name);
+    return launch_tc_expert(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T * k, k, E, I,
+                            H, 0, y, nullptr, ld_y, static_cast<cudaStream_t>(stream), name);
   MxArgs p{};
   p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
   p.w0 = wd; p.s0 = sd;

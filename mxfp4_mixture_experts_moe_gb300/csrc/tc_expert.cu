@@ -1,45 +1,48 @@
 // Tensor-core (tcgen05) path of the MXFP4 expert projections, used by the
 // stage calls for batches of more than 16 rows (prefill and large decode
-// batches; the 1-16-row exact-rows regime never takes it).
+// batches; the 1-16-row decode regime keeps the CUDA-core kernels).
 //
-// The layer's projections as grouped GEMMs, "DeepSeek-V4-Flash on AMD gfx90a",
-// §6.1 (packed FP4 weights with E8M0 block scales, INT8 per-32 activations)
-// and "Optimizing DeepSeek V4 Flash Inference on a Strix Halo Pair", "MXFP4
-// routed-expert kernels" (prefill tiles over the tokens of one expert).
-// Per expert e with n_e rows, out[row i][token t] = sum_k W[i][k] X[t][k]
-// with W the dequantised MXFP4 weights and X the dequantised Q8 activations.
+// The layer's projections as grouped GEMMs over the rows routed to each
+// expert: "DeepSeek-V4-Flash on AMD gfx90a", §6.1 (packed FP4 weights with
+// E8M0 block scales against INT8 per-32 activations: an exact integer dot
+// per block of 32, then activation and E8M0 scaling) and "Optimizing
+// DeepSeek V4 Flash Inference on a Strix Halo Pair", "MXFP4 routed-expert
+// kernels" (prefill tiles over the tokens of one expert).
 //
-// Operands (f16, tensor-core kind::f16, fp32 accumulation in tensor memory
-// over the whole reduction):
-//   A = E2M1 value * 2^(u - umax_i)   exact in f16 (umax_i = largest scale
-//       byte of weight row i in the tile; factors below 2^-24 flush to 0)
-//   B = Bhi + Blo, two f16 operands: v = q * sx / S_t (q the Q8 code, sx its
-//       block scale, S_t a power of two per token column with |v| <= 2^15),
-//       Bhi = f16(v), Blo = f16(v - Bhi): about 22 significant bits
-// and the epilogue multiplies by 2^(umax_i - 127) * S_t.  Unlike the
-// CUDA-core path there is no per-block integer dot here; the result differs
-// from the exact one by the tensor core's fp32 accumulation (relative
-// ~1e-5 on a 4096-term reduction) and B's residual.
+// Every block dot is exact, as in the CUDA-core kernels.  The tensor core
+// takes the weights as they are stored: E2M1 nibbles (kind::mxf4, K = 64 per
+// MMA = two MX blocks) with the weight's E8M0 byte as the block scale of A.
+// The Q8 codes q of the activations are not an MMA type, so each is written
+// as four signed base-4 digits q = d0 + 4 d1 + 16 d2 + 64 d3, d in
+// {-2..2} (every |q| <= 128 has such a form), each an exact E2M1 value;
+// plane i is an MMA operand with block scale 4^i.  The four plane MMAs sum
+// into one fp32 accumulator:  D = 2^(u-127) * sum_k v_k q_k = I_b 2^(u-128)
+// with I_b the integer block dot of twice the E2M1 values; every partial sum
+// is a multiple of 2^(u-128) below 2^(u-112), exact in fp32.  To keep the
+// two blocks of a K-step apart, the B operand has two rows per activation
+// row: rows [0, 32) carry the even block of each K-step (zeros in the odd
+// one), rows [32, 64) the odd block.  The epilogue of each K-step ("drain")
+// then forms  acc = fma(D, xs_b, acc)  per (weight row, activation row,
+// block), which equals the CUDA-core term fma(I_b, xs_b * 2^(u-128), acc):
+// the same exact product, one rounding.  Blocks are accumulated in
+// increasing order; the CUDA-core kernels add per-lane partial sums in a
+// butterfly instead, so the two paths agree within fp32 rounding, not bit
+// for bit.
 //
-// Tiles: 128 weight rows x up to 32 token columns of one expert, K in chunks
-// of 64 (two MX blocks); two MMAs (Bhi, Blo) per matrix and K step, A read
-// from tensor memory.  One persistent CTA per SM walks the tile list it
-// derives from the expert offsets, with warp-specialised roles:
-//   warps 0-15  widen the packed weights of one row and 64 K to f16 in
-//               registers and store them into a tensor-memory operand stage
-//               (tcgen05.st), one lane per weight row, in groups that take
-//               alternate chunks;
-//   warps 16-19 copy the token rows ahead (cp.async ring), write Bhi / Blo
-//               into a shared-memory operand stage, and drain the previous
-//               tile's accumulators (one TMEM lane quadrant each);
-//   warp 20     issues the tensor copies (TMA): 128 weight rows x 128 bytes
-//               (256 K) per copy, 128-byte swizzled, and the tile's scale
-//               bytes into a double buffer;
-//   warp 21     issues the MMAs;
-//   warp 22     builds the next tile's column tables (assignment, activation
-//               row, S_t) ahead of time.
-// Tensor memory holds two accumulator buffers (the epilogue of one tile
-// overlaps the next) and the A operand stages.
+// Tiles: 128 weight rows (MMA M) x up to 32 activation rows of one expert
+// (MMA N = 64), K in stages of 256 (8 blocks, 4 K-steps).  One persistent CTA
+// per SM walks the tiles it derives from the expert offsets:
+//   warps 0-7   drain: TMEM lane quadrant warp % 4, 16 activation rows each;
+//               fp32 accumulators in registers, epilogue (SwiGLU) and store
+//   warps 8-11  per stage: the digit planes of the stage's activation codes
+//               into shared memory (a 256-entry table per nibble position),
+//               the stage's activation scales, and the A block scales
+//               (E8M0 bytes of the weight rows) into tensor memory
+//   warp 12     tensor copies (TMA) of the packed weights, 128-byte swizzled
+//   warp 13     MMA issue
+//   warp 14     column tables of the next tile
+// Tensor memory: B scales (4 planes), a ring of A scales per stage slot, and
+// 3 (gate/up) or 6 (down) K-step accumulator buffers of 64 columns per matrix.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -51,105 +54,104 @@
 namespace moe {
 namespace {
 
-constexpr int kTcRows = 128;    // weight rows per tile (MMA M)
-constexpr int kTcCols = 32;     // token columns per tile, at most (MMA N)
-constexpr int kTcK = 64;        // reduction elements per chunk (one operand stage)
-constexpr int kTcSlice = 256;   // reduction elements per packed-weight copy (128-byte rows)
-constexpr int kAWarps = 16;     // weight converters
-constexpr int kBWarps = 4;      // token side and epilogue
-constexpr int kWarpProd = kAWarps + kBWarps;
-constexpr int kWarpMma = kWarpProd + 1;
+constexpr int kRows = 128;                     // weight rows per tile (MMA M)
+constexpr int kNT = 32;                        // activation rows per tile, at most
+constexpr int kN = 2 * kNT;                    // MMA N: even-block rows, then odd-block rows
+constexpr int kStageK = 256;                   // reduction elements per stage (8 MX blocks)
+constexpr int kSteps = kStageK / 64;           // MMA K-steps per stage
+constexpr int kPlanes = 4;                     // base-4 digit planes of the Q8 codes
+constexpr uint32_t kAMat = kRows * kStageK / 2;  // one matrix's packed weights per stage (16 KB)
+constexpr uint32_t kBPlane = kN * kStageK / 2;   // one digit plane per stage (8 KB)
+constexpr uint32_t kBStage = kPlanes * kBPlane;  // 32 KB
+constexpr uint32_t kXsStage = kNT * 8 * 4;       // activation scales of a stage (1 KB)
+constexpr int kDrainWarps = 8;
+constexpr int kPrepWarps = 4;
+constexpr int kWarpTma = kDrainWarps + kPrepWarps;
+constexpr int kWarpMma = kWarpTma + 1;
 constexpr int kWarpTab = kWarpMma + 1;
-constexpr int kTcThreads = 32 * (kWarpTab + 1);
-constexpr int kBThreads = 32 * kBWarps;
-constexpr int kBAhead = 6;      // token-row chunks in flight per token-side thread
-constexpr int kMaxA = 8;        // operand stages, at most
-constexpr int kMaxRaw = 8;      // packed-weight stages, at most
-constexpr uint32_t kRawMat = 128u * 128u;                     // one matrix's packed slice, 16 KB
-constexpr uint32_t kBStage = 2u * kTcCols * kTcK * 2u;        // Bhi + Blo of one chunk, 8 KB
-constexpr uint32_t kBRawSlot = (uint32_t)kBThreads * 20u;      // 16 code bytes + 1 scale per thread
-constexpr uint32_t kAccCols = 128;  // TMEM columns [0, 128): two accumulator buffers of 64
+constexpr int kThreads = 32 * (kWarpTab + 1);
+constexpr int kMaxStages = 4;
+constexpr int kMaxDBuf = 8;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaBase = 16;   // columns [0, 16): B scales, plane i at 4 i
+constexpr uint32_t kDBase = 128;    // first accumulator column
 
-static_assert(kBThreads == 4 * kTcCols, "one token-side thread per (column, 16-element piece)");
+enum Mode { kSwiglu = 0, kRaw = 1, kDownMode = 2 };
 
 struct TcArgs {
   const int8_t *aq;  // Q8 activation codes: x rows (gate/up, by token) or h rows (down, by assignment)
   int64_t ld_aq;
   const float *as;
   int64_t ld_as;
+  const uint8_t *s0, *s1;  // E8M0 bytes of the weight rows, [E*N][K/32]
   const int32_t *offsets, *sorted;
   int64_t cap;
   int A, k, E, K, N;  // K reduction length, N output rows per expert
   int bytoken;        // activation row of assignment a: a / k (1) or a (0)
   uint32_t kdiv;
-  float *out;
+  float *out0, *out1;
   int64_t ld_out;
   unsigned *status;
-  int as16;  // activation scale rows are 16-byte aligned
-  int nA;    // operand stages
-  int nraw;  // packed-weight stages
-  // shared memory (bytes from the 1024-aligned base)
-  uint32_t scale_buf;  // one tile's scale bytes (NM x 128 rows x K/32)
-  uint32_t off_scale, off_raw, off_b, off_braw, off_misc;
+  int nstage, ndbuf;
+  uint32_t off_a, off_b, off_xs, off_misc;  // shared memory (from the 1024-aligned base)
 };
 
-struct TcMaps {  // 2-D tensor maps (TMA) of the packed weights and their scale bytes
-  CUtensorMap w[2], s[2];
+struct TcMaps {  // 2-D tensor maps (TMA) of the packed weights
+  CUtensorMap w[2];
 };
 
 struct TcShared {
-  uint64_t raw_full[kMaxRaw], raw_empty[kMaxRaw];
-  uint64_t full[kMaxA], a_empty[kMaxA];
-  uint64_t acc_full[2], acc_empty[2], scale_full[2], scale_empty[2], tab_full[2], tab_empty[2], umax_full[3];
+  uint64_t a_full[kMaxStages], b_full[kMaxStages], slot_free[kMaxStages];
+  uint64_t d_full[kMaxDBuf], d_free[kMaxDBuf];
+  uint64_t tab_full[2], tab_empty[2];
   uint32_t tmem_slot;
-  int ncols[2], mtile[2];
-  int colrow[2][kTcCols], colasg[2][kTcCols];
-  float colS[2][kTcCols], colInv[2][kTcCols];
-  int umax[3][2 * kTcRows];  // largest scale byte of each weight row (matrix-major)
-  int prefix[1];             // [E + 1] tiles before expert e
+  int ncols[2];
+  int mrow[2];        // first output row of the tile within its expert
+  int64_t wrow[2];    // first weight row of the tile (expert * N + mrow)
+  int colrow[2][kNT]; // activation row of each column (-1: none)
+  int colasg[2][kNT]; // output row (assignment) of each column (-1: none)
+  uint32_t lut[2][256];  // Q8 code -> its four digit codes, low / high nibble of byte i = plane i
+  int prefix[1];         // [E + 1] tiles before expert e
 };
 
 uint32_t tc_shared_bytes(int E) { return (uint32_t)(sizeof(TcShared) + 4u * (uint32_t)E); }
 
-// f16 bits of 2^-d (d >= 0): normal down to 2^-14, subnormal to 2^-24, else 0.
-MOE_DEVFN uint32_t f16_pow2_neg(int d) {
-  if (d <= 14) return (uint32_t)(15 - d) << 10;
-  if (d <= 24) return 1u << (24 - d);
-  return 0u;
+// Shared-memory descriptor of a 128-byte swizzled K-major tile (8-row groups
+// 1024 bytes apart), as the tensor copies of the weights lay it out.
+MOE_DEVFN uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 
-// 2^(u - 127) as fp32 (u = 255: NaN).
-MOE_DEVFN float e8m0_value(int u) {
-  if (u >= 255) return __uint_as_float(0x7FC00000u);
-  if (u >= 1) return __uint_as_float((uint32_t)u << 23);
-  return __uint_as_float(0x00400000u);
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 block scales,
+// fp32 accumulator, both operands K-major), M x N.
+MOE_DEVFN uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Smallest power of two >= v for finite v > 0; 1 otherwise.
-MOE_DEVFN float pow2_ceil(float v) {
-  if (!(v > 0.0f) || !(v < 3.0e38f)) return 1.0f;
-  const uint32_t b = __float_as_uint(v);
-  const uint32_t e = b >> 23, man = b & 0x7FFFFFu;
-  if (e == 0) return __uint_as_float(0x00800000u);  // below the normal range: 2^-126
-  return __uint_as_float((e + (man != 0)) << 23);
+// D[tmem] (+)= A * B with per-32 block scales from tensor memory (sfa, sfb).
+MOE_DEVFN void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                        bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"((uint32_t)accumulate)
+      : "memory");
 }
 
-MOE_DEVFN uint32_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
+MOE_DEVFN void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
-// A box of 128 rows x nb bytes lands in shared memory with the tensor-copy
-// swizzle that matches its row length (nb = 128 / 64 / 32 bytes: 128B / 64B /
-// 32B swizzle, 16: none): the 16-byte chunk j of row r sits at chunk j ^ x(r).
-MOE_DEVFN uint32_t swz_of(int r, int nb) {
-  return nb == 128 ? (uint32_t)(r & 7) : nb == 64 ? (uint32_t)((r >> 1) & 3) : nb == 32 ? (uint32_t)((r >> 2) & 1) : 0u;
+MOE_DEVFN void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
-MOE_DEVFN uint32_t swz_addr(uint32_t base, int r, int byte, int nb, uint32_t x) {
-  return base + (uint32_t)r * (uint32_t)nb + ((((uint32_t)byte >> 4) ^ x) << 4) + ((uint32_t)byte & 15u);
-}
+MOE_DEVFN void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Bounded mbarrier wait taken by a whole warp, with one answer for all lanes.
 MOE_DEVFN bool warp_wait(uint32_t bar, uint32_t parity, unsigned *status) {
@@ -164,10 +166,32 @@ MOE_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, u
       : "memory");
 }
 
+// Balanced base-4 digits of a Q8 code (as its byte): q = d0 + 4 d1 + 16 d2 +
+// 64 d3 with d in {-2, .., 2}; digit codes are E2M1 (0 -> 0, +-1 -> 0x2 / 0xA,
+// +-2 -> 0x4 / 0xC).  Returns the four codes, plane i in nibble i.
+MOE_DEVFN uint32_t digit_codes(int q) {
+  uint32_t codes = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = q & 3;  // q mod 4 (two's complement)
+    const int d = r <= 1 ? r : (r == 3 ? -1 : (q > 0 ? 2 : -2));
+    const uint32_t c = d == 0 ? 0u : d == 1 ? 2u : d == 2 ? 4u : d == -1 ? 0xAu : 0xCu;
+    codes |= c << (4 * i);
+    q = (q - d) / 4;  // exact: q - d is a multiple of 4
+  }
+  return codes;
+}
+
+// Byte offset of (row r, byte j) of a no-swizzle K-major operand with 128-byte
+// rows: core matrices of 8 rows x 16 bytes, 128 bytes apart along K, 8-row
+// groups 1024 bytes apart.
+MOE_DEVFN uint32_t bofs(int r, int j) {
+  return (uint32_t)(r >> 3) * 1024u + (uint32_t)(j >> 4) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(j & 15);
+}
+
 struct Tile {
-  int e, mtile, ncols, ncol16;
-  int64_t row0;  // first weight row of the tile (expert e)
-  int col0;      // first sorted position of the tile
+  int e, mtile, ncols;
+  int col0;  // first sorted position of the tile
 };
 
 MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
@@ -184,26 +208,14 @@ MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   tl.mtile = local % mt;
   const int ntile = local / mt;
   const int b = p.offsets[lo], n_e = p.offsets[lo + 1] - b;
-  tl.col0 = b + ntile * kTcCols;
-  tl.ncols = min(kTcCols, n_e - ntile * kTcCols);
-  tl.ncol16 = (tl.ncols + 15) & ~15;
-  tl.row0 = (int64_t)lo * p.N + (int64_t)tl.mtile * kTcRows;
+  tl.col0 = b + ntile * kNT;
+  tl.ncols = min(kNT, n_e - ntile * kNT);
   return tl;
 }
 
-// Four packed bytes (8 weights) -> four f16x2 pairs scaled by f2.
-MOE_DEVFN void widen8(uint32_t w, uint32_t f2, uint32_t *o) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(f2));
-}
-
-template <int NM>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p, const __grid_constant__ TcMaps maps) {
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, const __grid_constant__ TcMaps maps) {
+  constexpr int NM = MODE == kDownMode ? 1 : 2;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
   const uint32_t dyn = smem_addr(smem_dyn);
   const uint32_t pad = ((dyn + 1023u) & ~1023u) - dyn;
@@ -212,30 +224,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
   TcShared &S = *reinterpret_cast<TcShared *>(smem + p.off_misc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int K = p.K, nb = K / 32, nchunk = K / kTcK, nslice = K / kTcSlice, mt = p.N / kTcRows;
-  const int nA = p.nA, nraw = p.nraw;
-  constexpr int NG = 4 / NM;  // converter groups (chunks c = group mod NG)
+  const int K = p.K, nstg = K / kStageK, mt = p.N / kRows;
+  const int NS = p.nstage, ND = p.ndbuf;
+  const uint32_t s_a = sb + p.off_a, s_b = sb + p.off_b, s_xs = sb + p.off_xs;
 
   if (tid == 0) {
-    for (int s = 0; s < nraw; ++s) {
-      mbar_init(smem_addr(&S.raw_full[s]), 1);
-      mbar_init(smem_addr(&S.raw_empty[s]), kAWarps);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&S.a_full[s]), 1);
+      mbar_init(smem_addr(&S.b_full[s]), kPrepWarps);
+      mbar_init(smem_addr(&S.slot_free[s]), 1 + kDrainWarps);
     }
-    for (int s = 0; s < nA; ++s) {
-      mbar_init(smem_addr(&S.full[s]), 4 * NM + kBWarps);
-      mbar_init(smem_addr(&S.a_empty[s]), 1);
+    for (int b = 0; b < ND; ++b) {
+      mbar_init(smem_addr(&S.d_full[b]), 1);
+      mbar_init(smem_addr(&S.d_free[b]), kDrainWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_addr(&S.acc_full[b]), 1);
-      mbar_init(smem_addr(&S.acc_empty[b]), kBWarps);
-      mbar_init(smem_addr(&S.scale_full[b]), 1);
-      mbar_init(smem_addr(&S.scale_empty[b]), kAWarps);
       mbar_init(smem_addr(&S.tab_full[b]), 1);
-      mbar_init(smem_addr(&S.tab_empty[b]), kBWarps);
+      mbar_init(smem_addr(&S.tab_empty[b]), kPrepWarps + kDrainWarps);
     }
-    for (int b = 0; b < 3; ++b) mbar_init(smem_addr(&S.umax_full[b]), 4 * NM);
     fence_mbar_init();
   }
+  // digit tables, and zeros in the operand halves that no stage ever writes
+  for (int i = tid; i < 256; i += kThreads) {
+    const uint32_t c = digit_codes((int)(int8_t)i);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int pl = 0; pl < 4; ++pl) {
+      const uint32_t d = (c >> (4 * pl)) & 0xFu;
+      lo |= d << (8 * pl);
+      hi |= d << (8 * pl + 4);
+    }
+    S.lut[0][i] = lo;
+    S.lut[1][i] = hi;
+  }
+  for (uint32_t o = 16u * tid; o < (uint32_t)NS * kBStage; o += 16u * kThreads) sts128(s_b + o, make_uint4(0, 0, 0, 0));
+  fence_proxy_async();
   if (warp == kWarpTab) {
     // tiles per expert, prefix-summed (every CTA derives the same list)
     int carry = 0;
@@ -247,7 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
         const int b = p.offsets[e], en = p.offsets[e + 1];
         const bool bad = b < 0 || en < b || en > p.cap;
         if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-        if (!bad && en > b) nt = ((en - b + kTcCols - 1) / kTcCols) * mt;
+        if (!bad && en > b) nt = ((en - b + kNT - 1) / kNT) * mt;
       }
       int incl = nt;
 #pragma unroll
@@ -264,240 +287,256 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&S.tmem_slot);
+  if (warp < 4) {
+    // B block scales: plane i = 4^i for both blocks of a K-step, every lane
+    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+#pragma unroll
+    for (int pl = 0; pl < kPlanes; ++pl)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st1(tmem + lanes + 4u * pl + c, 0x01010101u * (127u + 2u * pl));
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   const int ntiles = S.prefix[p.E];
   const int my_tiles = cta < ntiles ? (ntiles - cta + G - 1) / G : 0;
-  const uint32_t s_scale = sb + p.off_scale, s_raw = sb + p.off_raw, s_b = sb + p.off_b, s_braw = sb + p.off_braw;
 
-  if (warp < kAWarps) {
-    // ------------------------------------------------ weights -> tensor memory
-    const int grp = warp / (4 * NM), mm = NM == 2 ? (warp >> 2) & 1 : 0, q = warp & 3;
-    const int r = 32 * q + lane;  // weight row of the tile = TMEM lane
+  if (warp < kDrainWarps) {
+    // ------------------------------------------------ drain + epilogue
+    const int q = warp & 3, h = warp >> 2;
     const uint32_t lanes = (uint32_t)(32 * q) << 16;
-    const uint32_t xs = swz_of(r, nb), xr = (uint32_t)(r & 7);
-    for (int lt = 0; lt < my_tiles; ++lt) {
-      const int sbuf = lt & 1;
-      const uint32_t scl = s_scale + (uint32_t)sbuf * p.scale_buf + (uint32_t)mm * kTcRows * nb;
-      if (!warp_wait(smem_addr(&S.scale_full[sbuf]), (lt >> 1) & 1, p.status)) break;
-      uint32_t m4 = 0;
-      for (int j = 0; j < nb / 16; ++j) {
-        const uint4 v = lds128(swz_addr(scl, r, 16 * j, nb, xs));
-        m4 = __vmaxu4(__vmaxu4(m4, v.x), __vmaxu4(__vmaxu4(v.y, v.z), v.w));
-      }
-      const int umax = (int)max(max(m4 & 0xFFu, (m4 >> 8) & 0xFFu), max((m4 >> 16) & 0xFFu, m4 >> 24));
-      if (grp == 0) {
-        S.umax[lt % 3][mm * kTcRows + r] = umax;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&S.umax_full[lt % 3]));
-      }
-      bool dead = false;
-      for (int c = grp; c < nchunk; c += NG) {
-        const int g = lt * nchunk + c, s = g % nA;
-        const int J = lt * nslice + (c >> 2), rs = J % nraw;
-        if (!warp_wait(smem_addr(&S.raw_full[rs]), (J / nraw) & 1, p.status)) { dead = true; break; }
-        if (g >= nA && !warp_wait(smem_addr(&S.a_empty[s]), ((g / nA) - 1) & 1, p.status)) { dead = true; break; }
-        tc_fence_after();
-        const uint32_t row = s_raw + (uint32_t)rs * NM * kRawMat + (uint32_t)mm * kRawMat + (uint32_t)r * 128u;
-        const uint32_t j0 = 2u * (uint32_t)(c & 3);
-        const uint4 pa = lds128(row + ((j0 ^ xr) << 4));
-        const uint4 pb = lds128(row + (((j0 + 1u) ^ xr) << 4));
-        const uint32_t u2 = lds_u16(swz_addr(scl, r, 2 * c, nb, xs));
-        const uint32_t fa = f16_pow2_neg(umax - (int)(u2 & 0xFFu)), fb = f16_pow2_neg(umax - (int)(u2 >> 8));
-        const uint32_t fa2 = fa | (fa << 16), fb2 = fb | (fb << 16);
-        uint32_t o[32];
-        widen8(pa.x, fa2, o + 0);
-        widen8(pa.y, fa2, o + 4);
-        widen8(pa.z, fa2, o + 8);
-        widen8(pa.w, fa2, o + 12);
-        widen8(pb.x, fb2, o + 16);
-        widen8(pb.y, fb2, o + 20);
-        widen8(pb.z, fb2, o + 24);
-        widen8(pb.w, fb2, o + 28);
-        tmem_st32(tmem + lanes + kAccCols + (uint32_t)(s * NM + mm) * 32u, o);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_addr(&S.full[s]));
-          if ((c & 3) + NG >= 4) mbar_arrive(smem_addr(&S.raw_empty[rs]));  // this group's last chunk of the slice
-        }
-      }
-      if (dead) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.scale_empty[sbuf]));
-    }
-  } else if (warp < kWarpProd) {
-    // ------------------------------------------------ token side + epilogue
-    const int bt = tid - 32 * kAWarps, q = warp & 3;
-    const int cc = bt >> 2, pc = bt & 3;  // token column, 16-element piece of the chunk
-    const int total = my_tiles * nchunk;
-    bool dead = false;
-    auto issue = [&](int pos) {
-      if (pos < total) {
-        const int lt = pos / nchunk, c = pos - lt * nchunk, tb = lt & 1;
-        if (c == 0 && !warp_wait(smem_addr(&S.tab_full[tb]), (lt >> 1) & 1, p.status)) dead = true;
-        const int row = dead ? -1 : S.colrow[tb][cc];
-        if (row >= 0) {
-          const uint32_t slot = s_braw + (uint32_t)(pos % kBAhead) * kBRawSlot;
-          cp_async16(slot + 16u * bt, p.aq + (int64_t)row * p.ld_aq + c * kTcK + 16 * pc);
-          cp_async4(slot + 16u * kBThreads + 4u * bt, p.as + (int64_t)row * p.ld_as + 2 * c + (pc >> 1));
-        }
-      }
-      cp_async_commit();
-    };
-    auto epilogue = [&](int lt) {
-      const int ab = lt & 1, tb = lt & 1, u3 = lt % 3;
-      bool ok = warp_wait(smem_addr(&S.acc_full[ab]), (lt >> 1) & 1, p.status) &&
-                warp_wait(smem_addr(&S.umax_full[u3]), (lt / 3) & 1, p.status);
-      tc_fence_after();
-      const int i = 32 * q + lane;
-      const float rs0 = e8m0_value(S.umax[u3][i]);
-      const float rs1 = NM == 2 ? e8m0_value(S.umax[u3][kTcRows + i]) : 0.0f;
-      const int ncols = S.ncols[tb], ncol16 = (ncols + 15) & ~15;
-      const int64_t orow = (int64_t)S.mtile[tb] * kTcRows + i;
-      const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * 64u;
-      for (int cb = 0; ok && cb < ncol16; cb += 16) {
-        float d0[16];
-        tmem_ld16(acc + (uint32_t)cb, d0);
-        if (NM == 2) {
-          float d1[16];
-          tmem_ld16(acc + 32u + (uint32_t)cb, d1);
+    const int r = 32 * q + lane;  // weight row of the tile = TMEM lane
+    bool ok = true;
+    for (int lt = 0; lt < my_tiles && ok; ++lt) {
+      const int tb = lt & 1;
+      ok = warp_wait(smem_addr(&S.tab_full[tb]), (lt >> 1) & 1, p.status);
+      if (!ok) break;
+      const int ncols = S.ncols[tb];
+      const bool active = 16 * h < ncols;
+      float acc[NM][16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = cb + j;
-            const int a = col < ncols ? S.colasg[tb][col] : -1;
-            if (a >= 0) {
-              const float Sc = S.colS[tb][col];
-              const float gv = __fmul_rn(__fmul_rn(d0[j], rs0), Sc), uv = __fmul_rn(__fmul_rn(d1[j], rs1), Sc);
-              p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(silu(gv), uv);
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[m][c] = 0.0f;
+      for (int st = 0; st < nstg && ok; ++st) {
+        const int g = lt * nstg + st, slot = g % NS;
+        const uint32_t xsb = s_xs + (uint32_t)slot * kXsStage;
+        // the stage's activation scales are in place (the phase cannot move
+        // on before this warp releases the slot)
+        ok = warp_wait(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
+        if (!ok) break;
+        for (int s = 0; s < kSteps; ++s) {
+          const int j = g * kSteps + s, db = j % ND;
+          ok = warp_wait(smem_addr(&S.d_full[db]), (j / ND) & 1, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (active) {
+            const uint32_t dcol = tmem + lanes + kDBase + (uint32_t)db * NM * kN + 16u * h;
+            uint32_t de[NM][16], dd[NM][16];
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              tmem_ld16_nowait(dcol + (uint32_t)m * kN, de[m]);
+              tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd[m]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              // scales of blocks 8 st + 2 s and + 1 of column 16 h + c
+              uint32_t x0, x1;
+              asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                           : "=r"(x0), "=r"(x1)
+                           : "r"(xsb + (uint32_t)((16 * h + c) * 8 + 2 * s) * 4u));
+#pragma unroll
+              for (int m = 0; m < NM; ++m) {
+                acc[m][c] = __fmaf_rn(__uint_as_float(de[m][c]), __uint_as_float(x0), acc[m][c]);
+                acc[m][c] = __fmaf_rn(__uint_as_float(dd[m][c]), __uint_as_float(x1), acc[m][c]);
+              }
             }
           }
-        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&S.d_free[db]));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&S.slot_free[slot]));
+      }
+      if (ok && active) {
+        const int64_t orow = (int64_t)S.mrow[tb] + r;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = cb + j;
-            const int a = col < ncols ? S.colasg[tb][col] : -1;
-            if (a >= 0) p.out[(int64_t)a * p.ld_out + orow] = __fmul_rn(__fmul_rn(d0[j], rs0), S.colS[tb][col]);
+        for (int c = 0; c < 16; ++c) {
+          const int col = 16 * h + c;
+          const int a = col < ncols ? S.colasg[tb][col] : -1;
+          if (a >= 0) {
+            if (MODE == kSwiglu) p.out0[(int64_t)a * p.ld_out + orow] = __fmul_rn(silu(acc[0][c]), acc[NM - 1][c]);
+            else if (MODE == kRaw) {
+              p.out0[(int64_t)a * p.ld_out + orow] = acc[0][c];
+              p.out1[(int64_t)a * p.ld_out + orow] = acc[NM - 1][c];
+            } else {
+              p.out0[(int64_t)a * p.ld_out + orow] = acc[0][c];
+            }
           }
         }
       }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(&S.acc_empty[ab]));
-        mbar_arrive(smem_addr(&S.tab_empty[tb]));
-      }
-      return ok;
-    };
-    for (int j = 0; j < kBAhead - 1; ++j) issue(j);
-    for (int pos = 0; pos < total && !dead; ++pos) {
-      issue(pos + kBAhead - 1);
-      cp_async_wait<kBAhead - 1>();
-      const int lt = pos / nchunk, c = pos - lt * nchunk, tb = lt & 1;
-      const int s = pos % nA;
-      if (pos >= nA && !warp_wait(smem_addr(&S.a_empty[s]), ((pos / nA) - 1) & 1, p.status)) break;
-      const int ncols = S.ncols[tb], ncol16 = (ncols + 15) & ~15;
-      if (cc < ncol16) {
-        uint32_t hi[8], lo[8];
-        const int row = S.colrow[tb][cc];
-        if (cc < ncols && row >= 0) {
-          const uint32_t slot = s_braw + (uint32_t)(pos % kBAhead) * kBRawSlot;
-          const uint4 codes = lds128(slot + 16u * bt);
-          const float fac = __fmul_rn(lds_f32(slot + 16u * kBThreads + 4u * bt), S.colInv[tb][cc]);
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t wv = cw[i >> 1];
-            const int sh = 16 * (i & 1);
-            const float v0 = __fmul_rn((float)(int8_t)(wv >> sh), fac);
-            const float v1 = __fmul_rn((float)(int8_t)(wv >> (sh + 8)), fac);
-            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi[i]) : "f"(v1), "f"(v0));
-            float h0, h1;
-            asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
-                : "=f"(h0), "=f"(h1) : "r"(hi[i]));
-            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo[i]) : "f"(__fsub_rn(v1, h1)), "f"(__fsub_rn(v0, h0)));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0u;
-        }
-        const uint32_t st = s_b + (uint32_t)s * kBStage;
-        const uint32_t o0 = tile_offset(cc, 16 * pc), o1 = tile_offset(cc, 16 * pc + 8);
-        sts128(st + o0, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-        sts128(st + o1, make_uint4(hi[4], hi[5], hi[6], hi[7]));
-        sts128(st + kBStage / 2 + o0, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-        sts128(st + kBStage / 2 + o1, make_uint4(lo[4], lo[5], lo[6], lo[7]));
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.full[s]));
-      // the previous tile's accumulators, once this tile's first chunks are on their way
-      if (lt >= 1 && c == min(1, nchunk - 1) && !epilogue(lt - 1)) dead = true;
+      if (lane == 0) mbar_arrive(smem_addr(&S.tab_empty[tb]));
     }
-    cp_async_wait<0>();
-    if (!dead && my_tiles > 0) epilogue(my_tiles - 1);
-  } else if (warp == kWarpProd) {
-    // ------------------------------------------------ tensor copies
+  } else if (warp < kWarpTma) {
+    // ------------------------------------------------ digit planes, activation scales, A scales
+    const int q = warp & 3;
+    const uint32_t lanes = (uint32_t)(32 * q) << 16;
+    const int tp = tid - 32 * kDrainWarps;  // 0 .. 127
+    const int jb = tp & 7;                  // block of the stage this thread converts
+    const int nbk = K / 32;
+    bool ok = true;
+    for (int lt = 0; lt < my_tiles && ok; ++lt) {
+      const int tb = lt & 1;
+      ok = warp_wait(smem_addr(&S.tab_full[tb]), (lt >> 1) & 1, p.status);
+      if (!ok) break;
+      const int ncols = S.ncols[tb];
+      const int64_t wrow = S.wrow[tb] + 32 * q + lane;  // this lane's weight row (A scales)
+      int crow[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = (tp >> 3) + 16 * u;
+        crow[u] = c < ncols ? S.colrow[tb][c] : -1;
+      }
+      for (int st = 0; st < nstg && ok; ++st) {
+        const int g = lt * nstg + st, slot = g % NS;
+        // this stage's codes and scales (loaded before the slot is free)
+        uint4 code[2][2];
+        float xsv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (crow[u] >= 0) {
+            const int8_t *src = p.aq + (int64_t)crow[u] * p.ld_aq + st * kStageK + 32 * jb;
+            code[u][0] = ldg_nc(src);
+            code[u][1] = ldg_nc(src + 16);
+            xsv[u] = __ldg(p.as + (int64_t)crow[u] * p.ld_as + st * 8 + jb);
+          } else {
+            code[u][0] = code[u][1] = make_uint4(0, 0, 0, 0);
+            xsv[u] = 0.0f;
+          }
+        }
+        uint2 sfw[NM];
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+          sfw[m] = __ldg(reinterpret_cast<const uint2 *>((m == 0 ? p.s0 : p.s1) + wrow * nbk + st * 8));
+        if (g >= NS) {
+          ok = warp_wait(smem_addr(&S.slot_free[slot]), ((g / NS) - 1) & 1, p.status);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t bst = s_b + (uint32_t)slot * kBStage;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = (tp >> 3) + 16 * u;
+          if (crow[u] < 0) continue;
+          // 16 code pairs -> 16 words, byte i = plane i's byte of the pair
+          const uint32_t cw[8] = {code[u][0].x, code[u][0].y, code[u][0].z, code[u][0].w,
+                                  code[u][1].x, code[u][1].y, code[u][1].z, code[u][1].w};
+          uint32_t pw[4][4];  // [plane][word of 4 pairs]
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t v = cw[2 * g4 + (i >> 1)];
+              const int sh = 16 * (i & 1);
+              w[i] = S.lut[0][(v >> sh) & 0xFFu] | S.lut[1][(v >> (sh + 8)) & 0xFFu];
+            }
+            const uint32_t t0 = prmt(w[0], w[1], 0x5140u), t1 = prmt(w[0], w[1], 0x7362u);
+            const uint32_t t2 = prmt(w[2], w[3], 0x5140u), t3 = prmt(w[2], w[3], 0x7362u);
+            pw[0][g4] = prmt(t0, t2, 0x5410u);
+            pw[1][g4] = prmt(t0, t2, 0x7632u);
+            pw[2][g4] = prmt(t1, t3, 0x5410u);
+            pw[3][g4] = prmt(t1, t3, 0x7632u);
+          }
+          const int brow = (jb & 1) ? kNT + c : c;  // odd blocks go to the second half of the rows
+          const uint32_t off = bofs(brow, 16 * jb);
+#pragma unroll
+          for (int pl = 0; pl < kPlanes; ++pl)
+            sts128(bst + (uint32_t)pl * kBPlane + off, make_uint4(pw[pl][0], pw[pl][1], pw[pl][2], pw[pl][3]));
+          sts32(s_xs + (uint32_t)slot * kXsStage + (uint32_t)(c * 8 + jb) * 4u, __float_as_uint(xsv[u]));
+        }
+        // A block scales of the stage: K-step s of matrix m at columns
+        // kSfaBase + 4 (slot-local index) + quadrant, bytes 0 / 1 = its two blocks
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+#pragma unroll
+          for (int s = 0; s < kSteps; ++s) {
+            const uint32_t w2 = (s < 2 ? sfw[m].x : sfw[m].y) >> (16 * (s & 1));
+            const uint32_t col = kSfaBase + 4u * (uint32_t)((slot * kSteps + s) * NM + m) + (uint32_t)q;
+            tmem_st1(tmem + lanes + col, w2 & 0xFFFFu);
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&S.b_full[slot]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&S.tab_empty[tb]));
+    }
+  } else if (warp == kWarpTma) {
+    // ------------------------------------------------ tensor copies of the weights
     if (lane == 0) {
-      int J = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
         const Tile tl = tile_of(S, p, cta + lt * G, mt);
-        const int sbuf = lt & 1;
-        if (lt >= 2 && !mbar_wait(smem_addr(&S.scale_empty[sbuf]), ((lt >> 1) - 1) & 1, p.status)) break;
-        const uint32_t sbar = smem_addr(&S.scale_full[sbuf]);
-        mbar_arrive_expect_tx(sbar, (uint32_t)NM * kTcRows * nb);
-#pragma unroll
-        for (int mm = 0; mm < NM; ++mm)
-          tma_load_2d(s_scale + (uint32_t)sbuf * p.scale_buf + (uint32_t)mm * kTcRows * nb, &maps.s[mm], 0,
-                      (int)tl.row0, sbar);
-        bool dead = false;
-        for (int sl = 0; sl < nslice; ++sl, ++J) {
-          const int rs = J % nraw;
-          if (J >= nraw && !mbar_wait(smem_addr(&S.raw_empty[rs]), ((J / nraw) - 1) & 1, p.status)) {
-            dead = true;
+        const int row0 = tl.e * p.N + tl.mtile * kRows;
+        bool ok = true;
+        for (int st = 0; st < nstg; ++st) {
+          const int g = lt * nstg + st, slot = g % NS;
+          if (g >= NS && !mbar_wait(smem_addr(&S.slot_free[slot]), ((g / NS) - 1) & 1, p.status)) {
+            ok = false;
             break;
           }
-          const uint32_t bar = smem_addr(&S.raw_full[rs]);
-          mbar_arrive_expect_tx(bar, (uint32_t)NM * kRawMat);
+          const uint32_t bar = smem_addr(&S.a_full[slot]);
+          mbar_arrive_expect_tx(bar, (uint32_t)NM * kAMat);
 #pragma unroll
-          for (int mm = 0; mm < NM; ++mm)
-            tma_load_2d(s_raw + (uint32_t)(rs * NM + mm) * kRawMat, &maps.w[mm], sl * 128, (int)tl.row0, bar);
+          for (int m = 0; m < NM; ++m)
+            tma_load_2d(s_a + (uint32_t)(slot * NM + m) * kAMat, &maps.w[m], st * (kStageK / 2), row0, bar);
         }
-        if (dead) break;
+        if (!ok) break;
       }
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issue
     if (lane == 0) {
-      for (int lt = 0; lt < my_tiles; ++lt) {
-        const Tile tl = tile_of(S, p, cta + lt * G, mt);
-        const int ab = lt & 1;
-        if (lt >= 2 && !mbar_wait(smem_addr(&S.acc_empty[ab]), ((lt >> 1) - 1) & 1, p.status)) break;
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16(kTcRows, tl.ncol16);
-        bool ok = true;
-        for (int c = 0; c < nchunk; ++c) {
-          const int g = lt * nchunk + c, s = g % nA;
-          if (!mbar_wait(smem_addr(&S.full[s]), (g / nA) & 1, p.status)) {
-            ok = false;
-            break;
-          }
+      const uint32_t idesc = idesc_mxf4(kRows, kN);
+      bool ok = true;
+      for (int lt = 0; lt < my_tiles && ok; ++lt) {
+        for (int st = 0; st < nstg && ok; ++st) {
+          const int g = lt * nstg + st, slot = g % NS;
+          ok = mbar_wait(smem_addr(&S.a_full[slot]), (g / NS) & 1, p.status) &&
+               mbar_wait(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t bh = s_b + (uint32_t)s * kBStage, bl = bh + kBStage / 2;
-#pragma unroll
-          for (int mm = 0; mm < NM; ++mm) {
-            const uint32_t d = tmem + (uint32_t)ab * 64u + (uint32_t)mm * 32u;
-            const uint32_t a = tmem + kAccCols + (uint32_t)(s * NM + mm) * 32u;
-#pragma unroll
-            for (int ks = 0; ks < kTcK / 16; ++ks) {
-              mma_f16_ts(d, a + 8u * ks, smem_desc(bh + 256u * ks, kCoreLbo, kCoreSbo), idesc, c > 0 || ks > 0);
-              mma_f16_ts(d, a + 8u * ks, smem_desc(bl + 256u * ks, kCoreLbo, kCoreSbo), idesc, true);
+          for (int s = 0; s < kSteps; ++s) {
+            const int j = g * kSteps + s, db = j % ND;
+            if (j >= ND && !mbar_wait(smem_addr(&S.d_free[db]), ((j / ND) - 1) & 1, p.status)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              const uint32_t d = tmem + kDBase + (uint32_t)(db * NM + m) * kN;
+              const uint64_t ad = smem_desc_sw128(s_a + (uint32_t)(slot * NM + m) * kAMat + 32u * s);
+              const uint32_t sfa = tmem + kSfaBase + 4u * (uint32_t)((slot * kSteps + s) * NM + m);
+#pragma unroll
+              for (int pl = 0; pl < kPlanes; ++pl) {
+                const uint64_t bd = smem_desc(s_b + (uint32_t)slot * kBStage + (uint32_t)pl * kBPlane + 256u * s, 128u,
+                                              1024u);
+                mma_mxf4(d, ad, bd, idesc, sfa, tmem + 4u * pl, pl > 0);
+              }
+            }
+            mma_commit(smem_addr(&S.d_full[db]));
           }
-          mma_commit(smem_addr(&S.a_empty[s]));
+          if (ok) mma_commit(smem_addr(&S.slot_free[slot]));
         }
-        if (!ok) break;
-        mma_commit(smem_addr(&S.acc_full[ab]));
       }
     }
     __syncwarp();
@@ -516,38 +555,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(const TcArgs p
           a = -1;
         }
       }
-      const int row = a < 0 ? -1 : (p.bytoken ? token_of(a, p.kdiv) : a);
-      // the column's scale S_t: |q * sx| <= 127 * max sx; S_t scales the
-      // column into [-2^15, 2^15], the top of the f16 normal range, so that
-      // blocks far below the column's largest stay normal (full 11-bit
-      // precision in Bhi and Blo)
-      float mx = 0.0f;
-      if (row >= 0) {
-        const float *sp = p.as + (int64_t)row * p.ld_as;
-        if (p.as16) {
-          const float4 *s4 = reinterpret_cast<const float4 *>(sp);
-          for (int w = 0; w < nb / 4; ++w) {
-            const float4 v = __ldg(s4 + w);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-          }
-        } else {
-          for (int w = 0; w < nb; ++w) mx = fmaxf(mx, fabsf(__ldg(sp + w)));
-        }
-      }
-      const float Sc = __fmul_rn(pow2_ceil(127.0f * mx), 1.0f / 32768.0f);
       S.colasg[tb][c] = a;
-      S.colrow[tb][c] = row;
-      S.colS[tb][c] = Sc;
-      S.colInv[tb][c] = 1.0f / Sc;
+      S.colrow[tb][c] = a < 0 ? -1 : (p.bytoken ? token_of(a, p.kdiv) : a);
       if (lane == 0) {
         S.ncols[tb] = tl.ncols;
-        S.mtile[tb] = tl.mtile;
+        S.mrow[tb] = tl.mtile * kRows;
+        S.wrow[tb] = (int64_t)tl.e * p.N + tl.mtile * kRows;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&S.tab_full[tb]));
     }
   }
-  // every MMA of this CTA has completed (the last epilogue waited for it)
+  // every MMA of this CTA has completed (the drain waited for the last one)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -569,38 +588,38 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Row-major u8 matrix [rows][cols] (cols bytes per row) as a 2-D tensor map
-// with boxes of box_cols bytes x 128 rows, swizzled to match box_cols.
-bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols) {
+// Packed weights [rows][cols bytes] as a 2-D tensor map with boxes of 128
+// bytes x 128 rows, 128-byte swizzled.
+bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {box_cols, (cuuint32_t)kTcRows};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)kRows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle swz = box_cols == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
-                                 : box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                 : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-bool tc_expert_supported(int K, int N) { return K % 512 == 0 && K <= 4096 && N % kTcRows == 0; }
+bool tc_expert_supported(int K, int N) { return K % kStageK == 0 && K <= 8192 && N % kRows == 0; }
 
-// Launch of the tensor-core path (moe_mxfp4_gateup_swiglu / moe_mxfp4_down for
-// T > 16).  nm = 2: gate and up with SwiGLU; nm = 1: down.
-moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
+// Launch of the tensor-core path (moe_mxfp4_gateup_swiglu, moe_mxfp4_gateup
+// and moe_mxfp4_down for T > 16).  mode 0: gate and up with SwiGLU into out0;
+// 1: gate into out0, up into out1; 2: down into out0.
+moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
                             const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
-                            const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
-                            int K, int N, int bytoken, float *out, int64_t ld_out, cudaStream_t stream,
+                            const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E, int K,
+                            int N, int bytoken, float *out0, float *out1, int64_t ld_out, cudaStream_t stream,
                             const char *name) {
   if (!tc_expert_supported(K, N))
-    return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs K %% 512 == 0 (<= 4096) and rows %% 128 == 0", name);
+    return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs K %% 256 == 0 (<= 8192) and rows %% 128 == 0", name);
   if (E > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d", name, E);
+  if ((uintptr_t)s0 % 8 || (mode != kDownMode && (uintptr_t)s1 % 8))
+    return fail(MOE_ERR_INVALID_ARG, "%s: the tensor path needs 8-byte aligned scale bytes", name);
+  const int nm = mode == kDownMode ? 1 : 2;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, name);
@@ -608,54 +627,46 @@ moe_status launch_tc_expert(int nm, const int8_t *aq, int64_t ld_aq, const float
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   TcArgs p{};
   p.aq = aq; p.ld_aq = ld_aq; p.as = as; p.ld_as = ld_as;
+  p.s0 = s0; p.s1 = s1;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
   p.A = A; p.k = k; p.E = E; p.K = K; p.N = N; p.bytoken = bytoken;
   p.kdiv = kdiv_of(k);
-  p.out = out; p.ld_out = ld_out;
+  p.out0 = out0; p.out1 = out1; p.ld_out = ld_out;
   p.status = device_status_word();
-  p.as16 = ((uintptr_t)as % 16 == 0 && ld_as % 4 == 0) ? 1 : 0;
   TcMaps maps{};
   const uint64_t rows = (uint64_t)E * N;
-  for (int mm = 0; mm < nm; ++mm) {
-    if (!encode_rows(&maps.w[mm], mm == 0 ? w0 : w1, rows, (uint64_t)K / 2, 128u) ||
-        !encode_rows(&maps.s[mm], mm == 0 ? s0 : s1, rows, (uint64_t)K / 32, (uint32_t)(K / 32)))
-      return fail(MOE_ERR_UNSUPPORTED, "%s: tensor maps of the weights could not be built (16-byte aligned weights and scales are required)", name);
+  for (int m = 0; m < nm; ++m) {
+    if (!encode_rows(&maps.w[m], m == 0 ? w0 : w1, rows, (uint64_t)K / 2))
+      return fail(MOE_ERR_UNSUPPORTED, "%s: tensor maps of the weights could not be built (16-byte aligned weights are required)", name);
   }
-  // shared memory: two tile-scale buffers, the packed-weight ring, the
-  // operand (Bhi / Blo) ring, the token-row ring, small state.  Operand
-  // stages also take tensor memory (nm x 32 columns each, after the two
-  // accumulator buffers); packed-weight stages get what shared memory is left.
-  const uint32_t nb = (uint32_t)K / 32;
-  p.scale_buf = (uint32_t)nm * kTcRows * nb;
-  const int na_tmem = (int)((kTmemCols - kAccCols) / (32u * (uint32_t)nm));
-  const size_t fixed0 = 2u * (size_t)p.scale_buf + (size_t)kBAhead * kBRawSlot + tc_shared_bytes(E) + 1024u + 64u;
-  int nA = na_tmem < kMaxA ? na_tmem : kMaxA, nraw = 0;
-  const int min_a = 4 / nm + 1;
-  for (; nA >= min_a; --nA) {
-    const size_t fixed = fixed0 + (size_t)nA * kBStage;
-    nraw = fixed < (size_t)optin ? (int)(((size_t)optin - fixed) / ((size_t)nm * kRawMat)) : 0;
-    if (nraw >= 3) break;
-  }
-  if (nA < min_a) nA = min_a;
-  if (nraw > kMaxRaw) nraw = kMaxRaw;
-  if (nraw < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path does not fit shared memory", name);
-  p.nA = nA;
-  p.nraw = nraw;
-  p.off_scale = 0;
-  p.off_raw = 2u * p.scale_buf;  // a multiple of 1024 (swizzled copies land 1024-aligned)
-  p.off_b = p.off_raw + (uint32_t)nraw * nm * kRawMat;
-  p.off_braw = p.off_b + (uint32_t)nA * kBStage;
-  p.off_misc = (p.off_braw + (uint32_t)kBAhead * kBRawSlot + 63u) & ~63u;
+  // tensor memory: B scales [0, 16), A scales (4 columns per matrix and K-step
+  // of each stage slot) from 16, accumulators (64 columns per matrix) from 128
+  const int ns_tmem = (int)((kDBase - kSfaBase) / (4u * kSteps * (uint32_t)nm));
+  p.ndbuf = (int)((kTmemCols - kDBase) / (uint32_t)(nm * kN));
+  if (p.ndbuf > kMaxDBuf) p.ndbuf = kMaxDBuf;
+  // shared memory: the stage ring (packed weights, digit planes, activation
+  // scales), then the small state
+  const uint32_t stage = (uint32_t)nm * kAMat + kBStage + kXsStage;
+  const size_t fixed = (size_t)tc_shared_bytes(E) + 1024u + 64u;
+  int ns = (int)(((size_t)optin - fixed) / stage);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns > ns_tmem) ns = ns_tmem;
+  if (ns < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path does not fit shared memory", name);
+  p.nstage = ns;
+  p.off_a = 0;  // 1024-aligned (swizzled copies)
+  p.off_b = (uint32_t)ns * nm * kAMat;
+  p.off_xs = p.off_b + (uint32_t)ns * kBStage;
+  p.off_misc = (p.off_xs + (uint32_t)ns * kXsStage + 63u) & ~63u;
   const size_t smem = (size_t)p.off_misc + tc_shared_bytes(E) + 1024u;  // + alignment of the base
   if (smem > (size_t)optin) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs %zu bytes of shared memory", name, smem);
-  auto kern = nm == 2 ? tc_expert_kernel<2> : tc_expert_kernel<1>;
-  static bool configured[2][64] = {};
-  if (dev < 64 && !configured[nm - 1][dev]) {
+  auto kern = mode == kSwiglu ? tc_expert_kernel<kSwiglu> : mode == kRaw ? tc_expert_kernel<kRaw> : tc_expert_kernel<kDownMode>;
+  static bool configured[3][64] = {};
+  if (dev < 64 && !configured[mode][dev]) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (err != cudaSuccess) return cuda_fail(err, name);
-    configured[nm - 1][dev] = true;
+    configured[mode][dev] = true;
   }
-  kern<<<sm_count(), kTcThreads, smem, stream>>>(p, maps);
+  kern<<<sm_count(), kThreads, smem, stream>>>(p, maps);
   err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
 }

@@ -1,15 +1,17 @@
 """The tensor-core (tcgen05) expert projections, taken by the stage calls for
 batches of more than 16 rows, against the oracle.
 
-These GEMMs accumulate the whole reduction in fp32 on the tensor core with
-f16 operands: exact MXFP4 weights (E2M1 x a power of two per row) and the
-f16 rounding of the dequantised Q8 activations.  So the bar is the layer's
-floating-point tolerance, max|err| <= 1e-3 * RMS, not per-block bit
-identity (that bar, and the exact-rows contract, belong to 1-16 rows).
-Cases span several 128-row weight tiles, experts with more than 64 rows
-(several token tiles), experts with a handful of rows, padded segments, and
-reduction lengths from 512 to 4096 (the tensor path needs a multiple of
-512; other shapes keep the CUDA-core path).
+The tensor path keeps the layer's exact block dots: E2M1 weights with their
+E8M0 byte as the MMA block scale, the Q8 codes as four base-4 digit planes,
+one fp32 accumulator per block (exact), then acc = fma(D, xs, acc) block by
+block.  With unit scales every block term is an integer and every output is
+exact, so those cases are compared bit for bit with the oracle; with the
+layer's scales the order of the fp32 accumulation differs from the oracle's,
+so the bar is the layer's tolerance, max|err| <= 1e-3 * RMS.  Cases span
+several 128-row weight tiles, experts with more than 32 rows (several token
+tiles), experts with a handful of rows, padded segments, and reduction
+lengths from 256 to 4096 (the tensor path needs a multiple of 256; other
+shapes keep the CUDA-core path).
 """
 import numpy as np
 import pytest
@@ -92,9 +94,8 @@ def test_tensor_down(moe, H, I, E, k, T, tile):
 
 
 def test_tensor_path_large_activations(moe):
-    """Activations far beyond the f16 range (|x| ~ 1.3e5): the per-token power
-    of two S_t keeps the f16 operands in [-1, 1], so the result is still the
-    oracle's within tolerance."""
+    """Activation scales far from 1 (|x| ~ 1.3e5) are applied in fp32 after
+    the exact block dots, so the result is still the oracle's."""
     spec = synth.LayerSpec(H=512, E=2, k=1, I=128, seed=33)
     ex = {e: synth.expert(spec, e) for e in range(2)}
     T = 20
@@ -133,4 +134,43 @@ def test_sixteen_rows_keep_the_exact_path(moe):
                                     dev(srt), k, h)
         outs[T] = host(h)
     assert max_err_over_rms(outs[17][: 16 * k], outs[16]) <= 2 * TOL
+    assert moe.moe_device_status() == 0
+
+
+def _unit_scale_expert(spec, e):
+    """An expert of the spec with every E8M0 byte 128: each block term of the
+    projections is then the integer block dot itself."""
+    ex = synth.expert(spec, e)
+    for n in ("sg", "su", "sd"):
+        getattr(ex, n)[...] = 128
+    return ex
+
+
+@pytest.mark.parametrize("H,I,E,k,T", [(4096, 256, 3, 2, 70), (256, 128, 4, 3, 33)])
+def test_tensor_block_dots_exact(moe, H, I, E, k, T):
+    """Unit scales: gate/up (moe_mxfp4_gateup) and down outputs are sums of
+    exact integer block dots, equal to the oracle's bit for bit."""
+    spec = synth.LayerSpec(H=H, E=E, k=k, I=I, seed=35)
+    ex = {e: _unit_scale_expert(spec, e) for e in range(E)}
+    A = T * k
+    xq = synth.int8_codes(35, 2500, T, H)
+    xs = np.ones((T, H // 32), np.float32)
+    ids = _skewed_rows(T, k, E, 35, hot=1)
+    offsets, srt, _ = oracle.sort(ids, E, 1)
+    W = {n: _stack(ex, E, n) for n in ("wg", "sg", "wu", "su", "wd", "sd")}
+    g = torch.empty(A, I, device="cuda")
+    u = torch.empty(A, I, device="cuda")
+    moe.moe_mxfp4_gateup(dev(xq), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets), dev(srt), k, g, u)
+    hq = synth.int8_codes(35, 2501, A, I)
+    hs = np.ones((A, I // 32), np.float32)
+    y = torch.empty(A, H, device="cuda")
+    moe.moe_mxfp4_down(dev(hq), dev(hs), W["wd"], W["sd"], dev(offsets), dev(srt), T, k, y)
+    gg, uu, yy = host(g), host(u), host(y)
+    for a in range(A):
+        e = ex[ids.ravel()[a]]
+        go, uo = oracle.expert_gateup(xq[a // k], xs[a // k], e.wg, e.sg, e.wu, e.su)
+        assert np.array_equal(gg[a], go.astype(np.float32)), a
+        assert np.array_equal(uu[a], uo.astype(np.float32)), a
+        yo = oracle.expert_down(hq[a], hs[a], e.wd, e.sd)
+        assert np.array_equal(yy[a], yo.astype(np.float32)), a
     assert moe.moe_device_status() == 0
