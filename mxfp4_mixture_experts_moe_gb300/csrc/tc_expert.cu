@@ -13,12 +13,15 @@
 // takes the weights as they are stored: E2M1 nibbles (kind::mxf4, K = 64 per
 // MMA = two MX blocks) with the weight's E8M0 byte as the block scale of A.
 // The Q8 codes q of the activations are not an MMA type, so each is written
-// as four signed base-4 digits q = d0 + 4 d1 + 16 d2 + 64 d3, d in
-// {-2..2} (every |q| <= 128 has such a form), each an exact E2M1 value;
-// plane i is an MMA operand with block scale 4^i.  The four plane MMAs sum
-// into one fp32 accumulator:  D = 2^(u-127) * sum_k v_k q_k = I_b 2^(u-128)
-// with I_b the integer block dot of twice the E2M1 values; every partial sum
-// is a multiple of 2^(u-128) below 2^(u-112), exact in fp32.  To keep the
+// as three signed base-8 digits q = d0 + 8 d1 + 64 d2, d0, d1 in {-4..3} and
+// d2 in {-2..2} (every q in [-128, 127] has this form), each an exact E2M1
+// value; plane i is an MMA operand with block scale 8^i.  The three plane
+// MMAs sum into one fp32 accumulator:  D = 2^(u-127) * sum_k v_k q_k =
+// I_b 2^(u-128) with I_b the integer block dot of twice the E2M1 values;
+// every partial sum is a multiple of 2^(u-128) below 2^(u-110), exact in
+// fp32.  Every MMA accumulates (a block-scaled MMA that overwrites its
+// accumulator costs several times one that adds to it); the drain sets each
+// accumulator buffer back to zero after reading it.  To keep the
 // two blocks of a K-step apart, the B operand has two rows per activation
 // row: rows [0, 32) carry the even block of each K-step (zeros in the odd
 // one), rows [32, 64) the odd block.  The epilogue of each K-step ("drain")
@@ -41,7 +44,7 @@
 //   warp 12     tensor copies (TMA) of the packed weights, 128-byte swizzled
 //   warp 13     MMA issue
 //   warp 14     column tables of the next tile
-// Tensor memory: B scales (4 planes), a ring of A scales per stage slot, and
+// Tensor memory: B scales (3 planes), a ring of A scales per stage slot, and
 // 3 (gate/up) or 6 (down) K-step accumulator buffers of 64 columns per matrix.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -59,10 +62,10 @@ constexpr int kNT = 32;                        // activation rows per tile, at m
 constexpr int kN = 2 * kNT;                    // MMA N: even-block rows, then odd-block rows
 constexpr int kStageK = 256;                   // reduction elements per stage (8 MX blocks)
 constexpr int kSteps = kStageK / 64;           // MMA K-steps per stage
-constexpr int kPlanes = 4;                     // base-4 digit planes of the Q8 codes
+constexpr int kPlanes = 3;                     // base-8 digit planes of the Q8 codes
 constexpr uint32_t kAMat = kRows * kStageK / 2;  // one matrix's packed weights per stage (16 KB)
 constexpr uint32_t kBPlane = kN * kStageK / 2;   // one digit plane per stage (8 KB)
-constexpr uint32_t kBStage = kPlanes * kBPlane;  // 32 KB
+constexpr uint32_t kBStage = kPlanes * kBPlane;  // 24 KB
 constexpr uint32_t kXsStage = kNT * 8 * 4;       // activation scales of a stage (1 KB)
 constexpr int kDrainWarps = 8;
 constexpr int kPrepWarps = 4;
@@ -73,7 +76,7 @@ constexpr int kThreads = 32 * (kWarpTab + 1);
 constexpr int kMaxStages = 4;
 constexpr int kMaxDBuf = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaBase = 16;   // columns [0, 16): B scales, plane i at 4 i
+constexpr uint32_t kSfaBase = 16;   // columns [0, 12): B scales, plane i at 4 i
 constexpr uint32_t kDBase = 128;    // first accumulator column
 
 enum Mode { kSwiglu = 0, kRaw = 1, kDownMode = 2 };
@@ -143,6 +146,14 @@ MOE_DEVFN void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
+MOE_DEVFN void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 MOE_DEVFN void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -166,18 +177,19 @@ MOE_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, u
       : "memory");
 }
 
-// Balanced base-4 digits of a Q8 code (as its byte): q = d0 + 4 d1 + 16 d2 +
-// 64 d3 with d in {-2, .., 2}; digit codes are E2M1 (0 -> 0, +-1 -> 0x2 / 0xA,
-// +-2 -> 0x4 / 0xC).  Returns the four codes, plane i in nibble i.
+// Base-8 digits of a Q8 code (as its byte): q = d0 + 8 d1 + 64 d2 with d0,
+// d1 in {-4..3} and d2 in {-2..2}; digit codes are E2M1 (0 -> 0, 1 -> 0x2,
+// 2 -> 0x4, 3 -> 0x5, 4 -> 0x6, sign bit 0x8).  Returns the three codes,
+// plane i in nibble i.
 MOE_DEVFN uint32_t digit_codes(int q) {
   uint32_t codes = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = q & 3;  // q mod 4 (two's complement)
-    const int d = r <= 1 ? r : (r == 3 ? -1 : (q > 0 ? 2 : -2));
-    const uint32_t c = d == 0 ? 0u : d == 1 ? 2u : d == 2 ? 4u : d == -1 ? 0xAu : 0xCu;
-    codes |= c << (4 * i);
-    q = (q - d) / 4;  // exact: q - d is a multiple of 4
+  for (int i = 0; i < 3; ++i) {
+    const int d = i < 2 ? ((q + 4) & 7) - 4 : q;  // q is in [-2, 2] for the last digit
+    const int a = d < 0 ? -d : d;
+    const uint32_t mag = a == 0 ? 0u : a == 1 ? 2u : a == 2 ? 4u : a == 3 ? 5u : 6u;
+    codes |= (mag | (d < 0 ? 8u : 0u)) << (4 * i);
+    q = (q - d) >> 3;  // exact: q - d is a multiple of 8
   }
   return codes;
 }
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
     const uint32_t c = digit_codes((int)(int8_t)i);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
-    for (int pl = 0; pl < 4; ++pl) {
+    for (int pl = 0; pl < kPlanes; ++pl) {
       const uint32_t d = (c >> (4 * pl)) & 0xFu;
       lo |= d << (8 * pl);
       hi |= d << (8 * pl + 4);
@@ -288,12 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&S.tmem_slot);
   if (warp < 4) {
-    // B block scales: plane i = 4^i for both blocks of a K-step, every lane
+    // B block scales: plane i = 8^i for both blocks of a K-step, every lane
     const uint32_t lanes = (uint32_t)(32 * warp) << 16;
 #pragma unroll
     for (int pl = 0; pl < kPlanes; ++pl)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st1(tmem + lanes + 4u * pl + c, 0x01010101u * (127u + 2u * pl));
+      for (int c = 0; c < 4; ++c) tmem_st1(tmem + lanes + 4u * pl + c, 0x01010101u * (127u + 3u * pl));
+    // every accumulator column starts at zero (the MMAs only add)
+    const uint32_t zero[32] = {};
+    for (uint32_t c = kDBase; c < kTmemCols; c += 32) tmem_st32(tmem + lanes + c, zero);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -340,19 +355,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
               tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd[m]);
             }
             tmem_ld_wait();
+            // scales of blocks 8 st + 2 s and + 1 of columns 16 h .. 16 h + 15
+            float x0[16], x1[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 a = lds128(xsb + (uint32_t)((2 * s) * kNT + 16 * h + 4 * v) * 4u);
+              const uint4 b = lds128(xsb + (uint32_t)((2 * s + 1) * kNT + 16 * h + 4 * v) * 4u);
+              x0[4 * v] = __uint_as_float(a.x); x0[4 * v + 1] = __uint_as_float(a.y);
+              x0[4 * v + 2] = __uint_as_float(a.z); x0[4 * v + 3] = __uint_as_float(a.w);
+              x1[4 * v] = __uint_as_float(b.x); x1[4 * v + 1] = __uint_as_float(b.y);
+              x1[4 * v + 2] = __uint_as_float(b.z); x1[4 * v + 3] = __uint_as_float(b.w);
+            }
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              // scales of blocks 8 st + 2 s and + 1 of column 16 h + c
-              uint32_t x0, x1;
-              asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                           : "=r"(x0), "=r"(x1)
-                           : "r"(xsb + (uint32_t)((16 * h + c) * 8 + 2 * s) * 4u));
 #pragma unroll
               for (int m = 0; m < NM; ++m) {
-                acc[m][c] = __fmaf_rn(__uint_as_float(de[m][c]), __uint_as_float(x0), acc[m][c]);
-                acc[m][c] = __fmaf_rn(__uint_as_float(dd[m][c]), __uint_as_float(x1), acc[m][c]);
+                acc[m][c] = __fmaf_rn(__uint_as_float(de[m][c]), x0[c], acc[m][c]);
+                acc[m][c] = __fmaf_rn(__uint_as_float(dd[m][c]), x1[c], acc[m][c]);
               }
             }
+          }
+          {
+            // back to zero for the MMAs that add into this buffer next
+            const uint32_t zero[16] = {};
+            const uint32_t dz = tmem + lanes + kDBase + (uint32_t)db * NM * kN + 16u * h;
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              tmem_st16(dz + (uint32_t)m * kN, zero);
+              tmem_st16(dz + (uint32_t)m * kN + kNT, zero);
+            }
+            tmem_st_wait();
           }
           tc_fence_before();
           __syncwarp();
@@ -386,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
     const int q = warp & 3;
     const uint32_t lanes = (uint32_t)(32 * q) << 16;
     const int tp = tid - 32 * kDrainWarps;  // 0 .. 127
-    const int jb = tp & 7;                  // block of the stage this thread converts
+    const int jb = tp >> 4;                 // block of the stage this thread converts
+    // (lanes of an 8-lane phase take 8 consecutive rows of one block: their
+    // 16-byte plane stores fall in 8 distinct bank groups)
     const int nbk = K / 32;
     bool ok = true;
     for (int lt = 0; lt < my_tiles && ok; ++lt) {
@@ -398,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
       int crow[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int c = (tp >> 3) + 16 * u;
+        const int c = (tp & 15) + 16 * u;
         crow[u] = c < ncols ? S.colrow[tb][c] : -1;
       }
       for (int st = 0; st < nstg && ok; ++st) {
@@ -430,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         const uint32_t bst = s_b + (uint32_t)slot * kBStage;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int c = (tp >> 3) + 16 * u;
+          const int c = (tp & 15) + 16 * u;
           if (crow[u] < 0) continue;
           // 16 code pairs -> 16 words, byte i = plane i's byte of the pair
           const uint32_t cw[8] = {code[u][0].x, code[u][0].y, code[u][0].z, code[u][0].w,
@@ -457,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
 #pragma unroll
           for (int pl = 0; pl < kPlanes; ++pl)
             sts128(bst + (uint32_t)pl * kBPlane + off, make_uint4(pw[pl][0], pw[pl][1], pw[pl][2], pw[pl][3]));
-          sts32(s_xs + (uint32_t)slot * kXsStage + (uint32_t)(c * 8 + jb) * 4u, __float_as_uint(xsv[u]));
+          sts32(s_xs + (uint32_t)slot * kXsStage + (uint32_t)(jb * kNT + c) * 4u, __float_as_uint(xsv[u]));
         }
         // A block scales of the stage: K-step s of matrix m at columns
         // kSfaBase + 4 (slot-local index) + quadrant, bytes 0 / 1 = its two blocks
@@ -506,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
     // ------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t idesc = idesc_mxf4(kRows, kN);
+      const uint64_t adesc0 = smem_desc_sw128(s_a), bdesc0 = smem_desc(s_b, 128u, 1024u);
       bool ok = true;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
         for (int st = 0; st < nstg && ok; ++st) {
@@ -514,6 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
                mbar_wait(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
           if (!ok) break;
           tc_fence_after();
+          // descriptors of this stage; the MMAs below only add constant offsets
+          const uint64_t ad0 = adesc0 + (uint64_t)(((uint32_t)slot * NM * kAMat) >> 4);
+          const uint64_t bd0 = bdesc0 + (uint64_t)(((uint32_t)slot * kBStage) >> 4);
+          const uint32_t sfa0 = tmem + kSfaBase + 4u * (uint32_t)(slot * kSteps * NM);
+#pragma unroll
           for (int s = 0; s < kSteps; ++s) {
             const int j = g * kSteps + s, db = j % ND;
             if (j >= ND && !mbar_wait(smem_addr(&S.d_free[db]), ((j / ND) - 1) & 1, p.status)) {
@@ -521,18 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
               break;
             }
             tc_fence_after();
+            const uint32_t d0 = tmem + kDBase + (uint32_t)db * (NM * kN);
 #pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              const uint32_t d = tmem + kDBase + (uint32_t)(db * NM + m) * kN;
-              const uint64_t ad = smem_desc_sw128(s_a + (uint32_t)(slot * NM + m) * kAMat + 32u * s);
-              const uint32_t sfa = tmem + kSfaBase + 4u * (uint32_t)((slot * kSteps + s) * NM + m);
+            for (int pl = 0; pl < kPlanes; ++pl)
 #pragma unroll
-              for (int pl = 0; pl < kPlanes; ++pl) {
-                const uint64_t bd = smem_desc(s_b + (uint32_t)slot * kBStage + (uint32_t)pl * kBPlane + 256u * s, 128u,
-                                              1024u);
-                mma_mxf4(d, ad, bd, idesc, sfa, tmem + 4u * pl, pl > 0);
-              }
-            }
+              for (int m = 0; m < NM; ++m)
+                mma_mxf4(d0 + (uint32_t)m * kN, ad0 + (uint64_t)((m * kAMat + 32u * s) >> 4),
+                         bd0 + (uint64_t)((pl * kBPlane + 256u * s) >> 4), idesc, sfa0 + 4u * (uint32_t)(s * NM + m),
+                         tmem + 4u * pl, true);
             mma_commit(smem_addr(&S.d_full[db]));
           }
           if (ok) mma_commit(smem_addr(&S.slot_free[slot]));
