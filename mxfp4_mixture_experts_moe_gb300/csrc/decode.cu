@@ -456,29 +456,101 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     topk_group_stage(logit_s + t * E, p.bias, E, k, g, cand_key + u * k, cand_id + u * k);
   }
   __syncthreads();
-  if (warp < T) {
-    int id[8];
-    float wv[8];
-    topk_merge_stage(cand_key + warp * ngrp * k, cand_id + warp * ngrp * k, ngrp * k, k, id, wv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k && lane == j) {
-        m.ids[warp * k + j] = id[j];
-        m.w[warp * k + j] = wv[j];
-        if (cta == 0) {
-          p.ids[(int64_t)warp * k + j] = id[j];
-          p.weights[(int64_t)warp * k + j] = wv[j];
+  // the producer's copies of one gate/up slice into ring stage st (the whole
+  // producer warp calls it: the scale bytes may need per-lane copies)
+  const uint64_t pol = policy_evict_first();
+  const uint32_t gwb = (uint32_t)Rg * (H / 2), gsb = (uint32_t)Rg * nbH;
+  auto issue_gateup = [&](int st, int expert) {
+    const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
+    const uint32_t fb = smem_addr(&full[st]);
+    const int64_t row0 = (int64_t)expert * I + n0g;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(fb, 2 * gwb + (p.g16 ? 2 * gsb : 0u));
+      if (gwb > 0) {  // a CTA may own no gate/up rows when I < #SMs
+        bulk_g2s(sbase, p.wg + row0 * (H / 2), gwb, fb, pol);
+        bulk_g2s(sbase + p.gwreg, p.wu + row0 * (H / 2), gwb, fb, pol);
+        if (p.g16) {  // the slice's scale bytes are one contiguous 16-byte-aligned run
+          bulk_g2s(sbase + 2 * p.gwreg, p.sg + row0 * nbH, gsb, fb, pol);
+          bulk_g2s(sbase + 2 * p.gwreg + p.gsreg, p.su + row0 * nbH, gsb, fb, pol);
         }
       }
     }
-  }
-  if (T > 1) __syncthreads();  // one token: warp 0 wrote every id itself
-  else __syncwarp();
-  if (A <= 32) {
-    if (warp == 0) rank_sort_warp(m, A, E, cta == 0 ? p.status : nullptr);
+    if (!p.g16) {
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
+        const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
+        for (uint32_t c = lane; c < gsb / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+      }
+    }
+    cp_async_mbar_arrive_noinc(fb);
+  };
+  int early = 0;  // gate/up stages the producer already requested
+  if (T == 1) {
+    // one token: the producer warp merges, and requests slot j's gate/up slice
+    // as soon as slot j is decided; the ring takes the slots in score order
+    // (each expert has exactly one row, so no sort is needed)
+    if (warp == kCons) {
+      int id[8];
+      float wv[8];
+      auto pick = [&](int j, int e) {
+        if (j < nstage && e >= 0 && e < E) issue_gateup(j, e);
+      };
+      topk_merge_stage(cand_key, cand_id, ngrp * k, k, id, wv, pick);
+      bool valid = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k && lane == j) {
+          m.ids[j] = id[j];
+          m.w[j] = wv[j];
+          valid = id[j] >= 0 && id[j] < E;
+          if (valid) {
+            m.srt[j] = j;
+            m.skey[j] = id[j];
+            m.segb[j] = j;
+            m.active[j] = id[j];
+          } else if (cta == 0 && p.status) {
+            atomicOr(p.status, MOE_DEV_BAD_EXPERT_ID);
+          }
+          if (cta == 0) {
+            p.ids[j] = id[j];
+            p.weights[j] = wv[j];
+          }
+        }
+      }
+      // invalid slots (NaN scores) come last in score order
+      const int nv = __popc(__ballot_sync(0xffffffffu, valid));
+      if (lane == 0) {
+        m.segb[nv] = nv;
+        m.scalars[0] = nv;
+      }
+    }
     __syncthreads();
+    early = min(nstage, m.scalars[0]);
   } else {
-    rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
+    if (warp < T) {
+      int id[8];
+      float wv[8];
+      topk_merge_stage(cand_key + warp * ngrp * k, cand_id + warp * ngrp * k, ngrp * k, k, id, wv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k && lane == j) {
+          m.ids[warp * k + j] = id[j];
+          m.w[warp * k + j] = wv[j];
+          if (cta == 0) {
+            p.ids[(int64_t)warp * k + j] = id[j];
+            p.weights[(int64_t)warp * k + j] = wv[j];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (A <= 32) {
+      if (warp == 0) rank_sort_warp(m, A, E, cta == 0 ? p.status : nullptr);
+      __syncthreads();
+    } else {
+      rank_sort(m, A, E, cta == 0 ? p.status : nullptr);
+    }
   }
   const int nact = m.scalars[0];
   const int ndi = p.dpp == 2 ? (nact + 1) >> 1 : (nact + p.dpp - 1) / p.dpp;  // down ring items (dpp slots each)
@@ -488,37 +560,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     // ring, then its down slices, dpp slots per stage; once the first stages
     // are requested it asks for the down slices to be pulled into L2, so the
     // down copies (issued when gate/up stages free up) read from L2
-    const uint64_t pol = policy_evict_first();
-    const uint32_t gw = (uint32_t)Rg * (H / 2), gs = (uint32_t)Rg * nbH;
     const uint32_t dw = (uint32_t)Rd * (I / 2), ds = (uint32_t)Rd * nbI;
     const int first = nact < nstage ? nact : nstage;
-    int issued = 0;
-    for (int it = 0; it < nact + ndi; ++it) {
+    // once the first stages are requested, pull the down slices into L2
+    auto prefetch_down = [&]() {
+      if (dw > 0) {
+        for (int j = lane; j < nact; j += 32) {
+          const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + drow0 * (I / 2)), "r"(dw) : "memory");
+          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + drow0 * nbI), "r"(ds) : "memory");
+        }
+      }
+    };
+    if (early >= first) prefetch_down();
+    int issued = early;
+    for (int it = early; it < nact + ndi; ++it) {
       const int st = it % nstage;
       if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
       const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
       const uint32_t fb = smem_addr(&full[st]);
       if (it < nact) {
-        const int64_t row0 = (int64_t)m.active[it] * I + n0g;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, 2 * gw + (p.g16 ? 2 * gs : 0u));
-          if (gw > 0) {  // a CTA may own no gate/up rows when I < #SMs
-            bulk_g2s(sbase, p.wg + row0 * (H / 2), gw, fb, pol);
-            bulk_g2s(sbase + p.gwreg, p.wu + row0 * (H / 2), gw, fb, pol);
-            if (p.g16) {  // the slice's scale bytes are one contiguous 16-byte-aligned run
-              bulk_g2s(sbase + 2 * p.gwreg, p.sg + row0 * nbH, gs, fb, pol);
-              bulk_g2s(sbase + 2 * p.gwreg + p.gsreg, p.su + row0 * nbH, gs, fb, pol);
-            }
-          }
-        }
-        if (!p.g16) {
-#pragma unroll
-          for (int mm = 0; mm < 2; ++mm) {
-            const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
-            const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
-            for (uint32_t c = lane; c < gs / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
-          }
-        }
+        issue_gateup(st, m.active[it]);
       } else {
         const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
         if (lane == 0) {
@@ -539,16 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
             for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
           }
         }
+        cp_async_mbar_arrive_noinc(fb);
       }
-      cp_async_mbar_arrive_noinc(fb);
       issued = it + 1;
-      if (it == first - 1 && dw > 0) {
-        for (int j = lane; j < nact; j += 32) {
-          const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + drow0 * (I / 2)), "r"(dw) : "memory");
-          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + drow0 * nbI), "r"(ds) : "memory");
-        }
-      }
+      if (it == first - 1) prefetch_down();
     }
     for (int it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
       mbar_wait(smem_addr(&full[it % nstage]), (it / nstage) & 1, p.status);
@@ -562,10 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // when a group has written its h slice of expert slot j it counts that in
   // the workspace word of slot j.
   // Down: once every slot is counted by all CTAs, all consumer warps
-  // quantise every h row into the (now idle) ring area at once, then take
-  // units of two down rows of one slot, reading the weights from L2 (the
-  // producer prefetched them there), and leave y in shared memory for the
-  // combine.  A warp whose wait gave up stops computing but keeps arriving
+  // quantise every h row into shared memory at once (the region of Q8(x),
+  // no longer read), then the groups take the down ring items (dpp slots
+  // each, their slices already pulled into L2) in units of two rows of one
+  // slot, and leave y in shared memory for the combine.  A warp whose wait gave up stops computing but keeps arriving
   // on the ring and on the named barriers, so no other warp waits on it.
   const int grp = warp / kGroup, gw = warp - grp * kGroup;
   const int gbar = 3 + grp;  // named barrier of this group

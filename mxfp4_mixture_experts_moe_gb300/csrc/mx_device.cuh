@@ -223,9 +223,16 @@ MOE_DEVFN void topk_group_stage(const float *logits_row, const float *bias, int 
   }
 }
 
+struct NoPick {
+  MOE_DEVFN void operator()(int, int) const {}
+};
+
 // Stage 2: merge of n <= 64 (key, id) pairs into the k slots and weights
-// (every lane returns them).
-MOE_DEVFN void topk_merge_stage(const uint32_t *ck, const int *ci, int n, int k, int (&ids)[8], float (&w)[8]) {
+// (every lane returns them).  on_pick(j, id) is called by every lane as soon
+// as slot j is decided (id 0x7fffffff: only NaN scores were left).
+template <class Pick = NoPick>
+MOE_DEVFN void topk_merge_stage(const uint32_t *ck, const int *ci, int n, int k, int (&ids)[8], float (&w)[8],
+                                Pick on_pick = Pick()) {
   const int lane = threadIdx.x & 31;
   uint32_t ka = lane < n ? ck[lane] : 0u, kb = lane + 32 < n ? ck[lane + 32] : 0u;
   int ia = lane < n ? ci[lane] : 0x7fffffff, ib = lane + 32 < n ? ci[lane + 32] : 0x7fffffff;
@@ -249,6 +256,7 @@ MOE_DEVFN void topk_merge_stage(const uint32_t *ck, const int *ci, int n, int k,
       my_id = kmax ? win : 0x7fffffff;
       my_sel = kmax ? key_score(kmax) : -CUDART_INF_F;
     }
+    on_pick(j, kmax ? win : 0x7fffffff);
   }
   const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-my_sel)));
   float total = 0.0f;
