@@ -658,57 +658,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   }
 
   // ---- down phase
+  // once every slot is complete in every CTA (one warp polls the readiness
+  // words), all consumer warps quantise every h row into shared memory
   if (dead && lane == 0) m.scalars[4] = 1;
   bar_sync_named(1, kCons * 32);
   if (warp == 0) {
     bool ok = m.scalars[4] == 0;
     for (int j = lane; j < nact; j += 32) ok = ok && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
     ok = __all_sync(0xffffffffu, ok);
-    if (lane == 0) m.scalars[5] = ok;
+    if (lane == 0 && !ok) m.scalars[4] = 1;
   }
   bar_sync_named(1, kCons * 32);
-  const bool hdead = m.scalars[5] == 0;
+  dead = m.scalars[4] != 0;  // one answer for the whole CTA from here on
   const uint32_t hq = smem_addr(smem + p.off_hq);  // Q8(h) rows by sorted position
   const int nq = m.segb[nact];
-  if (!hdead) {
-    // Q8 of every h row, two blocks per lane pair and pass (loads first)
-    const int ntask = 2 * nq * nbI;  // (row, block, half)
-    for (int idx0 = warp * 64; idx0 < ntask; idx0 += kCons * 64) {
-      float v[2][16];
-      bool valid[2];
-      int ql[2], b[2];
+  if (!dead) {
+    const int ntask = 2 * nq * nbI;  // (row, block, half), one per lane
+#pragma unroll 1
+    for (int c = warp; 32 * c < ntask; c += kCons) {
+      const int idx = 32 * c + lane;
+      const bool valid = idx < ntask;
+      const int blk = valid ? idx >> 1 : 0;
+      const int ql = blk / nbI, b = blk - ql * nbI;
+      const float *src = p.h + (int64_t)m.srt[ql] * p.ld_h + 32 * b + 16 * (idx & 1);
+      float v[16];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int idx = idx0 + 32 * u + lane;
-        valid[u] = idx < ntask;
-        const int blk = valid[u] ? idx >> 1 : 0;
-        ql[u] = blk / nbI;
-        b[u] = blk - ql[u] * nbI;
-        const float *src = p.h + (int64_t)m.srt[ql[u]] * p.ld_h + 32 * b[u] + 16 * (idx & 1);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 r = valid[u] ? ldcg_v4(src + 4 * c) : make_uint4(0, 0, 0, 0);
-          v[u][4 * c] = __uint_as_float(r.x);
-          v[u][4 * c + 1] = __uint_as_float(r.y);
-          v[u][4 * c + 2] = __uint_as_float(r.z);
-          v[u][4 * c + 3] = __uint_as_float(r.w);
-        }
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 r = valid ? ldcg_v4(src + 4 * q4) : make_uint4(0, 0, 0, 0);
+        v[4 * q4] = __uint_as_float(r.x);
+        v[4 * q4 + 1] = __uint_as_float(r.y);
+        v[4 * q4 + 2] = __uint_as_float(r.z);
+        v[4 * q4 + 3] = __uint_as_float(r.w);
       }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) q8_pair_to_row(v[u], lane & 1, valid[u], hq + (uint32_t)ql[u] * p.hrow, I, b[u]);
+      q8_pair_to_row(v, lane & 1, valid, hq + (uint32_t)ql * p.hrow, I, b);
     }
   }
   bar_sync_named(1, kCons * 32);
-  dead = dead || hdead;
-  // down ring items: the groups keep alternating items (item it, slots
-  // (it - nact) * dpp ...); a unit is two rows of one slot sharing the
-  // activation loads
-  for (int it = nact + ((grp - nact) % 2 + 2) % 2; it < nact + ndi; it += 2) {
+  // down ring items: every consumer warp takes every item; group g computes
+  // the item's slots g, g + 2, ... (a unit is two rows of one slot sharing
+  // the activation loads), then group 0 releases the stage
+  for (int it = nact; it < nact + ndi; ++it) {
     const int st = it % nstage;
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     if (!dead) {
       const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
-      for (int j = j0; j < j1; ++j) {
+      for (int j = j0 + grp; j < j1; j += 2) {
         const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes) + (uint32_t)(j - j0) * p.dslot;
         const int sb = m.segb[j], se = m.segb[j + 1];
 #pragma unroll 1
@@ -736,8 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+    bar_sync_named(1, kCons * 32);
+    if (grp == 0 && lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
   bar_sync_named(1, kCons * 32);
   // combine of this CTA's output slice, slot order
