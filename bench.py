@@ -55,6 +55,14 @@ WORKLOADS = {
 }
 METRIC = "MoE-layer tokens/s and achieved HBM TB/s (decode 1–16 rows; prefill 512 rows)"
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# roofline kernel, from one ncu capture of the current kernels on a one-layer
+# copy of the workload; workloads without a capture report null.
+NCU_TRAFFIC = {
+    ("decode-1", "moe_decode_forward"): 84.02e6,
+    ("prefill-512", "moe_mxfp4_gateup_swiglu"): 2.3207e9,
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -439,8 +447,9 @@ def main():
     if gu_ms:
         gb = sum(gu_bytes[s % NG] for s in gu_steps)
         achieved = gb / (sum(gu_ms) * 1e-3) / 1e9
-        roofline = {"kernel": "moe_decode_forward" if fused else "moe_mxfp4_gateup_swiglu", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                    "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+        rk = "moe_decode_forward" if fused else "moe_mxfp4_gateup_swiglu"
+        roofline = {"kernel": rk, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                    "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get((args.workload, rk)),
                     "peak_kind": peak_kind, "launches_timed": len(gu_ms),
                     "avg_launch_us": 1e3 * sum(gu_ms) / len(gu_ms),
                     "algorithmic_bytes_per_launch": gb / len(gu_ms)}
