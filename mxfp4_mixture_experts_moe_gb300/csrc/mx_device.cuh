@@ -444,15 +444,16 @@ MOE_DEVFN void row_dot_smem_packed(uint32_t row, int K, const uint4 (&wr)[NM][S]
 // positive codes and 0 for negative ones, neg the reverse, so that
 // dot(x, 2v) = dot(x, pos) - dot(x, neg).  One byte-permute lookup per 4
 // codes and sign (a set selector top bit replicates the table byte's zero sign
-// bit); the high halves come down with umulhi, which runs on the multiply
-// pipe instead of the integer-logic pipe.  For weights used by one row.
+// bit); the high halves come down with shifts on the integer-logic pipe (the
+// multiply pipe is already the busier one: it carries the dp4a).  For weights
+// used by one row.
 MOE_DEVFN void e2m1x8_pos_neg(uint32_t w, uint32_t &p_lo, uint32_t &p_hi, uint32_t &n_lo, uint32_t &n_hi) {
   const uint32_t T0 = 0x03020100u, T1 = 0x0C080604u;  // {0,1,2,3 | 4,6,8,12}
   const uint32_t wx = w ^ 0x88888888u;
   p_lo = prmt(T0, T1, w);
-  p_hi = prmt(T0, T1, __umulhi(w, 0x10000u));
+  p_hi = prmt(T0, T1, w >> 16);
   n_lo = prmt(T0, T1, wx);
-  n_hi = prmt(T0, T1, __umulhi(wx, 0x10000u));
+  n_hi = prmt(T0, T1, wx >> 16);
 }
 
 // row_dot_smem with packed weights decoded by sign (no block sums needed).
