@@ -435,27 +435,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         const int c = (tp & 15) + 16 * u;
         crow[u] = c < ncols ? S.colrow[tb][c] : -1;
       }
-      for (int st = 0; st < nstg && ok; ++st) {
-        const int g = lt * nstg + st, slot = g % NS;
-        // this stage's codes and scales (loaded before the slot is free)
-        uint4 code[2][2];
-        float xsv[2];
+      // a stage's codes and scales are loaded one stage ahead, so their
+      // latency overlaps the conversion of the stage before
+      uint4 code[2][2];
+      float xsv[2];
+      uint2 sfw[NM];
+      auto load_stage = [&](int st, uint4 (&cd)[2][2], float (&xv)[2], uint2 (&sf)[NM]) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          if (crow[u] >= 0) {
+          if (crow[u] >= 0 && st < nstg) {
             const int8_t *src = p.aq + (int64_t)crow[u] * p.ld_aq + st * kStageK + 32 * jb;
-            code[u][0] = ldg_nc(src);
-            code[u][1] = ldg_nc(src + 16);
-            xsv[u] = __ldg(p.as + (int64_t)crow[u] * p.ld_as + st * 8 + jb);
+            cd[u][0] = ldg_nc(src);
+            cd[u][1] = ldg_nc(src + 16);
+            xv[u] = __ldg(p.as + (int64_t)crow[u] * p.ld_as + st * 8 + jb);
           } else {
-            code[u][0] = code[u][1] = make_uint4(0, 0, 0, 0);
-            xsv[u] = 0.0f;
+            cd[u][0] = cd[u][1] = make_uint4(0, 0, 0, 0);
+            xv[u] = 0.0f;
           }
         }
-        uint2 sfw[NM];
 #pragma unroll
         for (int m = 0; m < NM; ++m)
-          sfw[m] = __ldg(reinterpret_cast<const uint2 *>((m == 0 ? p.s0 : p.s1) + wrow * nbk + st * 8));
+          sf[m] = st < nstg ? __ldg(reinterpret_cast<const uint2 *>((m == 0 ? p.s0 : p.s1) + wrow * nbk + st * 8))
+                            : make_uint2(0, 0);
+      };
+      load_stage(0, code, xsv, sfw);
+      for (int st = 0; st < nstg && ok; ++st) {
+        const int g = lt * nstg + st, slot = g % NS;
+        uint4 ncode[2][2];
+        float nxsv[2];
+        uint2 nsfw[NM];
+        load_stage(st + 1, ncode, nxsv, nsfw);
         if (g >= NS) {
           ok = warp_wait(smem_addr(&S.slot_free[slot]), ((g / NS) - 1) & 1, p.status);
           if (!ok) break;
@@ -509,6 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&S.b_full[slot]));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          code[u][0] = ncode[u][0];
+          code[u][1] = ncode[u][1];
+          xsv[u] = nxsv[u];
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) sfw[m] = nsfw[m];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&S.tab_empty[tb]));
