@@ -63,6 +63,7 @@ def lib():
             L.moe_oracle_layer.argtypes = ([P, C.c_int, C.c_int, C.c_int, P, C.c_int, P, C.c_int, C.c_int, C.c_int]
                                            + [P] * 6 + [P] * 10)
             L.moe_oracle_layer.restype = C.c_int
+            L.moe_oracle_shared_expert.argtypes = [P, P, C.c_int, C.c_int, C.c_int] + [P] * 6 + [P] * 5
             _lib = L
     return _lib
 
@@ -175,11 +176,34 @@ def combine(y: np.ndarray, w: np.ndarray) -> np.ndarray:
     return out
 
 
-def layer(x: np.ndarray, wr: np.ndarray, bias, k: int, experts: dict):
+def shared_expert(xq, xs, ew, out=None):
+    """The shared expert on the Q8 rows xq [T, H] / xs [T, H/32]: ``ew`` has
+    wg, sg, wu, su, wd, sd arrays of one expert.  Returns a dict with h, hq,
+    hs and ys [T, H] (f64) and, when ``out`` (the routed output [T, H]) is
+    given, the joined output routed + ys."""
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xs = np.ascontiguousarray(xs, dtype=np.float32)
+    T, H = xq.shape
+    I = ew.wg.shape[0]
+    arrs = [np.ascontiguousarray(getattr(ew, n), dtype=np.uint8) for n in ("wg", "sg", "wu", "su", "wd", "sd")]
+    r = dict(h=np.empty((T, I), np.float64), hq=np.empty((T, I), np.int8), hs=np.empty((T, I // 32), np.float32),
+             ys=np.empty((T, H), np.float64))
+    joined = None if out is None else np.array(out, dtype=np.float64, copy=True, order="C")
+    lib().moe_oracle_shared_expert(_p(xq), _p(xs), T, H, I, *[_p(a) for a in arrs], _p(r["h"]), _p(r["hq"]),
+                                   _p(r["hs"]), _p(r["ys"]), None if joined is None else _p(joined))
+    if joined is not None:
+        r["out"] = joined
+    return r
+
+
+def layer(x: np.ndarray, wr: np.ndarray, bias, k: int, experts: dict, shared=None):
     """Full layer for the T tokens of x.  ``experts`` maps an expert id to an
     object with wg, sg, wu, su, wd, sd arrays (only the selected experts are
     needed; use :func:`route` first to know which).  Returns a dict of every
-    stage: logits, ids, w, xq, xs, h, hq, hs, y, out."""
+    stage: logits, ids, w, xq, xs, h, hq, hs, y, out.  With ``shared`` (one
+    expert's arrays) the shared expert joins: out is then routed + shared,
+    out_routed the routed part, and shared_h / shared_hq / shared_hs / ys the
+    shared expert's stages."""
     x = np.ascontiguousarray(x)
     wr = np.ascontiguousarray(wr)
     T, H = x.shape
@@ -211,6 +235,11 @@ def layer(x: np.ndarray, wr: np.ndarray, bias, k: int, experts: dict):
         _p(r["h"]), _p(r["hq"]), _p(r["hs"]), _p(r["y"]), _p(r["out"]))
     if rc != 0:
         raise KeyError("a selected expert's weights were not provided")
+    if shared is not None:
+        sr = shared_expert(r["xq"], r["xs"], shared, out=r["out"])
+        r["out_routed"] = r["out"]
+        r["out"] = sr["out"]
+        r.update(shared_h=sr["h"], shared_hq=sr["hq"], shared_hs=sr["hs"], ys=sr["ys"])
     return r
 
 

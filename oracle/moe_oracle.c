@@ -344,3 +344,40 @@ int moe_oracle_layer(const void *x, int x_bf16, int T, int H,
     free(hf);
     return rc;
 }
+
+/* ------------------------------------------------------------------ shared expert */
+
+/* The shared expert ([GFX] Execution structure and Fig. 1: the layer has a
+ * shared expert beside the routed experts, and both feed the join that adds
+ * their partials).  READING: the pages give neither the shared expert's
+ * weight format nor the join's arithmetic.  This build takes one expert in
+ * the routed experts' MXFP4 format and shape, run on the same Q8(x) rows
+ * with weight 1 -- per token the steps of one routed assignment: gate/up +
+ * SwiGLU -> Q8(h) -> down -- and the join out[t] = routed[t] + ys[t].
+ *   xq [T,H], xs [T,H/32]: Q8 of the tokens (as moe_oracle_layer's);
+ *   h [T,I] f64, hq [T,I], hs [T,I/32] f32, ys [T,H] f64: outputs;
+ *   out [T,H] f64: the routed output on entry, the joined output on return
+ *   (NULL: ys only). */
+void moe_oracle_shared_expert(const int8_t *xq, const float *xs, int T, int H, int I,
+                              const uint8_t *wg, const uint8_t *sg, const uint8_t *wu, const uint8_t *su,
+                              const uint8_t *wd, const uint8_t *sd,
+                              double *h, int8_t *hq, float *hs, double *ys, double *out)
+{
+    double *G = (double *)malloc(sizeof(double) * (size_t)I);
+    double *U = (double *)malloc(sizeof(double) * (size_t)I);
+    float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+    for (int t = 0; t < T; ++t) {
+        moe_oracle_expert_gateup(xq + (int64_t)t * H, xs + (int64_t)t * (H / 32), wg, sg, wu, su, H, I, G, U);
+        for (int i = 0; i < I; ++i) {
+            h[(int64_t)t * I + i] = moe_oracle_silu(G[i]) * U[i];
+            hf[i] = (float)h[(int64_t)t * I + i];
+        }
+        moe_oracle_quant_q8(hf, 0, 1, I, I, hq + (int64_t)t * I, I, hs + (int64_t)t * (I / 32), I / 32);
+        moe_oracle_expert_down(hq + (int64_t)t * I, hs + (int64_t)t * (I / 32), wd, sd, H, I, ys + (int64_t)t * H);
+        if (out)
+            for (int n = 0; n < H; ++n) out[(int64_t)t * H + n] += ys[(int64_t)t * H + n];
+    }
+    free(G);
+    free(U);
+    free(hf);
+}

@@ -38,6 +38,7 @@ S_ROUTER = 1
 S_X = 2
 S_PERM = 3
 S_EXPERT0 = 16  # expert e, tensor j in [0, 6): S_EXPERT0 + 8 * e + j
+S_SHARED0 = 8   # the shared expert, tensor j in [0, 6): S_SHARED0 + j
 T_WG, T_SG, T_WU, T_SU, T_WD, T_SD = range(6)
 
 
@@ -173,6 +174,20 @@ def expert(spec: LayerSpec, e: int) -> ExpertWeights:
         su=e8m0_bytes(s, base + T_SU, I * H // 32).reshape(I, H // 32),
         wd=random_bytes(s, base + T_WD, H * I // 2).reshape(H, I // 2),
         sd=e8m0_bytes(s, base + T_SD, H * I // 32).reshape(H, I // 32),
+    )
+
+
+def shared_expert(spec: LayerSpec) -> ExpertWeights:
+    """The layer's shared expert: the routed experts' format and shape, drawn
+    from its own streams."""
+    H, I, s = spec.H, spec.I, spec.seed
+    return ExpertWeights(
+        wg=random_bytes(s, S_SHARED0 + T_WG, I * H // 2).reshape(I, H // 2),
+        sg=e8m0_bytes(s, S_SHARED0 + T_SG, I * H // 32).reshape(I, H // 32),
+        wu=random_bytes(s, S_SHARED0 + T_WU, I * H // 2).reshape(I, H // 2),
+        su=e8m0_bytes(s, S_SHARED0 + T_SU, I * H // 32).reshape(I, H // 32),
+        wd=random_bytes(s, S_SHARED0 + T_WD, H * I // 2).reshape(H, I // 2),
+        sd=e8m0_bytes(s, S_SHARED0 + T_SD, H * I // 32).reshape(H, I // 32),
     )
 
 

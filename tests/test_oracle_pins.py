@@ -373,3 +373,67 @@ def test_layer_token_permutation_is_exact():
     assert np.array_equal(rp["ids"], r["ids"][perm])
     aperm = (perm[:, None] * spec.k + np.arange(spec.k)[None]).ravel()
     assert np.array_equal(rp["hq"], r["hq"][aperm])
+
+
+# --------------------------------------------------------------- shared expert
+
+def test_shared_expert_matches_textbook_dense_expert():
+    # the shared expert written out with dense fp64 matrices: G, U = W x,
+    # h = silu(G) U, y = Wd Q8(h), joined onto the routed output
+    from scipy.special import expit
+    spec = synth.TINY
+    x = synth.activations(spec, 3)
+    wr = synth.router_weights(spec)
+    experts = {e: synth.expert(spec, e) for e in range(spec.E)}
+    sh = synth.shared_expert(spec)
+    r = oracle.layer(x, wr, None, spec.k, experts, shared=sh)
+    xd = _dequant_q8(*oracle.quant_q8(x))
+    ys = np.empty((3, spec.H))
+    for t in range(3):
+        G = _dequant_weights(sh.wg, sh.sg) @ xd[t]
+        U = _dequant_weights(sh.wu, sh.su) @ xd[t]
+        h = G * expit(G) * U
+        hq, hs = oracle.quant_q8(h.astype(np.float32)[None])
+        ys[t] = _dequant_weights(sh.wd, sh.sd) @ _dequant_q8(hq, hs)[0]
+    rms = np.sqrt(np.mean(ys ** 2))
+    assert np.max(np.abs(r["ys"] - ys)) <= 1e-6 * rms
+    assert np.array_equal(r["out"], r["out_routed"] + r["ys"])
+    assert not np.array_equal(r["out"], r["out_routed"])
+
+
+def test_shared_expert_is_a_one_expert_routed_layer():
+    # a routed layer with one expert and k = 1 gives that expert weight
+    # sigmoid(l) / sigmoid(l) = 1, so its output is the shared expert's
+    spec = synth.TINY
+    x = synth.activations(spec, 4)
+    sh = synth.shared_expert(spec)
+    r1 = oracle.layer(x, np.ones((1, spec.H), np.float32), None, 1, {0: sh})
+    assert np.all(r1["w"] == 1.0)
+    s = oracle.shared_expert(r1["xq"], r1["xs"], sh)
+    assert np.array_equal(s["ys"], r1["out"])
+    assert np.array_equal(s["hq"], r1["hq"]) and np.array_equal(s["hs"], r1["hs"])
+
+
+def test_shared_expert_zero_down_weights_leave_the_routed_output():
+    spec = synth.TINY
+    x = synth.activations(spec, 2)
+    wr = synth.router_weights(spec)
+    experts = {e: synth.expert(spec, e) for e in range(spec.E)}
+    sh = synth.shared_expert(spec)
+    sh.wd[...] = 0
+    r = oracle.layer(x, wr, None, spec.k, experts, shared=sh)
+    assert np.all(r["ys"] == 0.0)
+    assert np.array_equal(r["out"], r["out_routed"])
+
+
+def test_shared_expert_down_sign_flip_negates_exactly():
+    # flipping the sign bit of every down nibble negates every block dot
+    spec = synth.TINY
+    x = synth.activations(spec, 2)
+    xq, xs = oracle.quant_q8(x)
+    sh = synth.shared_expert(spec)
+    a = oracle.shared_expert(xq, xs, sh)
+    sh.wd ^= 0x88
+    b = oracle.shared_expert(xq, xs, sh)
+    assert np.array_equal(b["ys"], -a["ys"])
+    assert np.array_equal(b["hq"], a["hq"])
