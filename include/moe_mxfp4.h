@@ -11,6 +11,9 @@
  *   moe_mxfp4_down           y = Wd h per assignment
  *   moe_combine              out[t] = sum_j w[t,j] * y[t*k+j], slot order
  *
+ * and, for a layer with a shared expert, the stage calls on its one-expert
+ * weight set followed by moe_join_add (out += ys).
+ *
  * It follows the layer as the DeepSeek-V4-Flash pages describe it:
  *  - "DeepSeek-V4-Flash on AMD gfx90a: Correctness Recovery and Inference
  *    Performance Engineering": Fig. 1 (router top-6 -> routed experts gate/up ->
@@ -203,6 +206,24 @@ MOE_API moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *
  *  y [T*k][ld_y], w [T][k] fp32; out [T][ld_out] fp32 output. */
 MOE_API moe_status moe_combine(const float *y, int64_t ld_y, const float *w, int T, int k, int H,
                        float *out, int64_t ld_out, void *stream);
+
+/* ---------------------------------------------------------------- shared expert */
+
+/* The join of the shared expert ("DeepSeek-V4-Flash on AMD gfx90a", Execution
+ * structure and Fig. 1: a shared expert beside the routed experts, both
+ * feeding a join that adds their partials): out[t,n] = out[t,n] + ys[t,n],
+ * fp32, one rounding.  The shared expert itself is the stage calls above on
+ * a one-expert weight set (E = 1, k = 1, offsets {0, T}, sorted 0..T-1):
+ * the layer's Q8(x) rows -> moe_mxfp4_gateup_swiglu -> act_quant_q8 ->
+ * moe_mxfp4_down -> ys; the pages give neither the shared expert's weight
+ * format nor the join's arithmetic, and this is the plainest reading that
+ * keeps the routed experts' arithmetic.
+ *  ys  [T][ld_ys] fp32 (device, read); out [T][ld_out] fp32 (device, read and
+ *      written; the routed output on entry).
+ * Errors: MOE_ERR_INVALID_ARG for T < 0, H <= 0, null pointers or ld < H
+ * (nothing is launched); T = 0 is a no-op. */
+MOE_API moe_status moe_join_add(const float *ys, int64_t ld_ys, int T, int H, float *out, int64_t ld_out,
+                                void *stream);
 
 /* ---------------------------------------------------------------- fused decode */
 

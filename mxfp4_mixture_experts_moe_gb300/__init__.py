@@ -27,7 +27,7 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
-           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_decode_workspace_bytes",
+           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_join_add", "moe_decode_workspace_bytes",
            "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc"]
 
 _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
@@ -43,6 +43,7 @@ _SIG = {
     "moe_mxfp4_gateup": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _P, _L, _P]),
     "moe_mxfp4_down": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _L, _P]),
     "moe_combine": (_I, [_P, _L, _P, _I, _I, _I, _P, _L, _P]),
+    "moe_join_add": (_I, [_P, _L, _I, _I, _P, _L, _P]),
     "moe_decode_workspace_bytes": (C.c_size_t, []),
     "moe_decode_max_tokens": (_I, [_I, _I, _I, _I]),
     "moe_decode_forward": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L] + [_P] * 3
@@ -184,6 +185,12 @@ def moe_combine(y, w, out, stream=None):
     _check(_lib.moe_combine(_ptr(y), _ld(y), _ptr(w), T, k, H, _ptr(out), _ld(out), _stream(stream)))
 
 
+def moe_join_add(ys, out, stream=None):
+    """out += ys (the shared expert's join onto the routed output)."""
+    T, H = out.shape
+    _check(_lib.moe_join_add(_ptr(ys), _ld(ys), T, H, _ptr(out), _ld(out), _stream(stream)))
+
+
 def moe_decode_workspace_bytes() -> int:
     return _lib.moe_decode_workspace_bytes()
 
@@ -218,4 +225,4 @@ def moe_decode_forward_noalloc(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out
                                            I, _ptr(out), _ld(out), _stream(stream)))
 
 
-from .layer import MoeLayer, LayerWeights, Workspace  # noqa: E402
+from .layer import MoeLayer, LayerWeights, SharedExpertWeights, Workspace  # noqa: E402

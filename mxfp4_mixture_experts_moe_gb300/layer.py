@@ -2,8 +2,10 @@
 
 The layer of the DeepSeek-V4-Flash pages ("DeepSeek-V4-Flash on AMD gfx90a",
 Fig. 1): route top-k -> sort -> Q8(x) -> gate/up + SwiGLU -> Q8(h) -> down ->
-slot-ordered combine.  This module only allocates device buffers (through
-PyTorch) and issues the calls; it computes nothing itself.
+slot-ordered combine, and, when the layer has a shared expert, that expert on
+every token (weight 1) joined onto the routed output.  This module only
+allocates device buffers (through PyTorch) and issues the calls; it computes
+nothing itself.
 """
 from __future__ import annotations
 
@@ -12,7 +14,20 @@ import dataclasses
 import torch
 
 from . import (act_quant_q8, moe_combine, moe_decode_forward, moe_decode_max_tokens, moe_decode_workspace_bytes,
-               moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens, moe_sort_tokens_capacity)
+               moe_join_add, moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens,
+               moe_sort_tokens_capacity)
+
+
+@dataclasses.dataclass
+class SharedExpertWeights:
+    """The layer's shared expert as a one-expert weight set in the boundary
+    layout of the routed experts, run on every token with weight 1."""
+    wg: torch.Tensor  # [1, I, H/2] uint8
+    sg: torch.Tensor  # [1, I, H/32] uint8
+    wu: torch.Tensor
+    su: torch.Tensor
+    wd: torch.Tensor  # [1, H, I/2] uint8
+    sd: torch.Tensor  # [1, H, I/32] uint8
 
 
 @dataclasses.dataclass
@@ -27,6 +42,7 @@ class LayerWeights:
     wd: torch.Tensor            # [E, H, I/2] uint8
     sd: torch.Tensor            # [E, H, I/32] uint8
     k: int
+    shared: SharedExpertWeights | None = None
 
     @property
     def E(self):
@@ -42,8 +58,11 @@ class LayerWeights:
 
     @property
     def nbytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in
-                   (self.wr, self.wg, self.sg, self.wu, self.su, self.wd, self.sd))
+        ts = [self.wr, self.wg, self.sg, self.wu, self.su, self.wd, self.sd]
+        if self.shared is not None:
+            sh = self.shared
+            ts += [sh.wg, sh.sg, sh.wu, sh.su, sh.wd, sh.sd]
+        return sum(t.numel() * t.element_size() for t in ts)
 
 
 class Workspace:
@@ -82,6 +101,14 @@ class Workspace:
         # grid-barrier counters of the fused decode path (zero-filled once)
         nws = (moe_decode_workspace_bytes() + 7) // 8
         self.decode_ws = torch.zeros(nws, dtype=torch.int64, device=device)
+        if lw.shared is not None:
+            # the shared expert's stages: one expert holding every token in order
+            self.sh_offsets = torch.tensor([0, T], dtype=torch.int32, device=device)
+            self.sh_sorted = torch.arange(max(T, 1), dtype=torch.int32, device=device)
+            self.sh_h = buf(T, I, torch.float32)
+            self.sh_hq = buf(T, I, torch.int8, 16)
+            self.sh_hs = buf(T, I // 32, torch.float32)
+            self.sh_y = buf(T, H, torch.float32)
 
 
 class MoeLayer:
@@ -105,20 +132,15 @@ class MoeLayer:
     def forward(self, x: torch.Tensor, ws: Workspace, stream=None, events: dict | None = None) -> torch.Tensor:
         """out = MoE(x) for the T rows of x ([T, H] bf16/f32, unit column stride).
 
-        ``events`` optionally maps a stage name ("route", "sort", "quant_x",
-        "gateup", "quant_h", "down", "combine") to a (start, end) pair of
-        torch.cuda.Event recorded around that stage on ``stream``."""
+        ``events`` optionally maps a stage name ("decode" for the single-launch
+        path; "route", "sort", "quant_x", "gateup", "quant_h", "down",
+        "combine" for the stage calls; "shared_quant_x", "shared_gateup",
+        "shared_quant_h", "shared_down", "join" for the shared expert) to a
+        (start, end) pair of torch.cuda.Event recorded around that stage on
+        ``stream``."""
         lw = self.lw
         s = torch.cuda.current_stream() if stream is None else stream
         ev = events or {}
-        if self.use_fused(ws.T):
-            if "decode" in ev:
-                ev["decode"][0].record(s)
-            moe_decode_forward(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, lw.k, ws.out, ws.logits,
-                               ws.ids, ws.w, ws.h, ws.y, ws.decode_ws, stream=s)
-            if "decode" in ev:
-                ev["decode"][1].record(s)
-            return ws.out
 
         def stage(name, fn, *args):
             if name in ev:
@@ -127,16 +149,40 @@ class MoeLayer:
             if name in ev:
                 ev[name][1].record(s)
 
-        stage("route", moe_route_topk, x, lw.wr, lw.bias, lw.k, ws.logits, ws.ids, ws.w)
-        stage("sort", moe_sort_tokens, ws.ids, lw.E, ws.tile_rows, ws.offsets, ws.sorted, ws.inv)
-        stage("quant_x", act_quant_q8, x, ws.xq, ws.xs)
-        stage("gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, lw.wg, lw.sg, lw.wu, lw.su, ws.offsets, ws.sorted,
-              lw.k, ws.h)
-        stage("quant_h", act_quant_q8, ws.h, ws.hq, ws.hs)
-        stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
-        stage("combine", moe_combine, ws.y, ws.w, ws.out)
+        fused = self.use_fused(ws.T)
+        if fused:
+            if "decode" in ev:
+                ev["decode"][0].record(s)
+            moe_decode_forward(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, lw.k, ws.out, ws.logits,
+                               ws.ids, ws.w, ws.h, ws.y, ws.decode_ws, stream=s)
+            if "decode" in ev:
+                ev["decode"][1].record(s)
+        else:
+            stage("route", moe_route_topk, x, lw.wr, lw.bias, lw.k, ws.logits, ws.ids, ws.w)
+            stage("sort", moe_sort_tokens, ws.ids, lw.E, ws.tile_rows, ws.offsets, ws.sorted, ws.inv)
+            stage("quant_x", act_quant_q8, x, ws.xq, ws.xs)
+            stage("gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, lw.wg, lw.sg, lw.wu, lw.su, ws.offsets, ws.sorted,
+                  lw.k, ws.h)
+            stage("quant_h", act_quant_q8, ws.h, ws.hq, ws.hs)
+            stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
+            stage("combine", moe_combine, ws.y, ws.w, ws.out)
+        sh = lw.shared
+        if sh is not None:
+            # the shared expert: the stage calls on its one-expert weight set
+            # (every token, weight 1), then its join onto the routed output
+            if fused:
+                stage("shared_quant_x", act_quant_q8, x, ws.xq, ws.xs)
+            stage("shared_gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, sh.wg, sh.sg, sh.wu, sh.su, ws.sh_offsets,
+                  ws.sh_sorted, 1, ws.sh_h)
+            stage("shared_quant_h", act_quant_q8, ws.sh_h, ws.sh_hq, ws.sh_hs)
+            stage("shared_down", moe_mxfp4_down, ws.sh_hq, ws.sh_hs, sh.wd, sh.sd, ws.sh_offsets, ws.sh_sorted, ws.T,
+                  1, ws.sh_y)
+            stage("join", moe_join_add, ws.sh_y, ws.out)
         return ws.out
 
     def kernels_per_forward(self, T: int) -> int:
         """Launches of this library's kernels per forward."""
-        return 1 if self.use_fused(T) else 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
+        n = 1 if self.use_fused(T) else 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
+        if self.lw.shared is not None:
+            n += 5 if self.use_fused(T) else 4  # (quant x), gate/up, quant h, down, join
+        return n

@@ -80,6 +80,10 @@ def test_host_validation_rejects_bad_arguments(lib):
         moe.MOE_ERR_INVALID_ARG
     # combine: output stride shorter than H
     assert lib.moe_combine(p, 64, p, 1, 2, 64, p, 32, None) == moe.MOE_ERR_INVALID_ARG
+    # shared-expert join: stride shorter than H, null output, negative T
+    assert lib.moe_join_add(p, 32, 1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_join_add(p, 64, 1, 64, None, 64, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_join_add(p, 64, -1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_empty_batch_is_a_host_noop(lib):
@@ -88,5 +92,6 @@ def test_empty_batch_is_a_host_noop(lib):
     assert lib.moe_route_topk(None, 1, 256, None, 1, None, 0, 256, 8, 2, None, None, None, None) == moe.MOE_OK
     assert lib.act_quant_q8(None, 0, 0, 64, 64, None, 64, None, 2, None) == moe.MOE_OK
     assert lib.moe_combine(None, 64, None, 0, 2, 64, None, 64, None) == moe.MOE_OK
+    assert lib.moe_join_add(None, 64, 0, 64, None, 64, None) == moe.MOE_OK
     assert lib.moe_mxfp4_down(None, 16, None, 1, None, None, None, None, 0, 0, 6, 256, 4096, 2048, None, 4096,
                               None) == moe.MOE_OK
