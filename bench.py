@@ -76,6 +76,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="layer copies to cycle (default: per workload)")
     ap.add_argument("--graph-steps", type=int, default=16, help="layer forwards captured per CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the cpu_baseline sample")
+    ap.add_argument("--shared-expert", action="store_true",
+                    help="the layer also has a shared expert (every token, weight 1, joined onto the routed output)")
     return ap.parse_args()
 
 
@@ -140,8 +142,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_layer(moe, torch, seed, zipf, device):
-    """Random-init layer in the boundary layout, generated on the device."""
+def make_layer(moe, torch, seed, zipf, device, shared=False):
+    """Random-init layer in the boundary layout, generated on the device
+    (with a shared expert of the same format when ``shared``)."""
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     wr = (torch.randn(E, H, generator=g, device=device) * 0.02).to(torch.bfloat16)
@@ -159,10 +162,15 @@ def make_layer(moe, torch, seed, zipf, device):
     def sc(*shape):
         return (123 + torch.randint(0, 5, shape, generator=g, device=device)).to(torch.uint8)
 
+    sh = None
+    if shared:
+        sh = moe.SharedExpertWeights(wg=nib(1, I_EXP, H // 2), sg=sc(1, I_EXP, H // 32),
+                                     wu=nib(1, I_EXP, H // 2), su=sc(1, I_EXP, H // 32),
+                                     wd=nib(1, H, I_EXP // 2), sd=sc(1, H, I_EXP // 32))
     return moe.LayerWeights(wr=wr, bias=bias, k=K_TOP,
                             wg=nib(E, I_EXP, H // 2), sg=sc(E, I_EXP, H // 32),
                             wu=nib(E, I_EXP, H // 2), su=sc(E, I_EXP, H // 32),
-                            wd=nib(E, H, I_EXP // 2), sd=sc(E, H, I_EXP // 32))
+                            wd=nib(E, H, I_EXP // 2), sd=sc(E, H, I_EXP // 32), shared=sh)
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -171,7 +179,7 @@ class OracleSample:
     """The CPU oracle on a pool of tokens of the same workload (inputs from the
     seeded generator), timed per assignment so any step budget can be met."""
 
-    def __init__(self, T, zipf, pool=8):
+    def __init__(self, T, zipf, pool=8, shared=False):
         import oracle
         import synth
         self.oracle, self.synth = oracle, synth
@@ -182,23 +190,26 @@ class OracleSample:
         self.bias = synth.router_bias(self.spec)
         _, self.ids, _ = oracle.route(self.x, self.wr, self.k, self.bias)
         self.experts = {int(e): synth.expert(self.spec, int(e)) for e in np.unique(self.ids)}
+        self.shared = synth.shared_expert(self.spec) if shared else None
+        self.units = self.k + (1 if shared else 0)  # expert passes per token
         self.pool = pool
         self.T = T
 
     def run_assignments(self, n_assign, start=0):
-        """One token through the oracle: the whole layer when n_assign == k,
-        else routing, Q8(x) and n_assign of its slots (gate/up, SwiGLU, Q8(h),
-        down).  Returns seconds."""
+        """One token through the oracle: the whole layer (with the shared
+        expert, if any) when n_assign == units, else routing, Q8(x) and
+        n_assign of its routed slots (gate/up, SwiGLU, Q8(h), down).  Returns
+        seconds."""
         o = self.oracle
         t = start % self.pool
         xt = self.x[t:t + 1]
         t0 = time.perf_counter()
-        if n_assign >= self.k:
-            o.layer(xt, self.wr, self.bias, self.k, self.experts)
+        if n_assign >= self.units:
+            o.layer(xt, self.wr, self.bias, self.k, self.experts, shared=self.shared)
             return time.perf_counter() - t0
         _, ids, _ = o.route(xt, self.wr, self.k, self.bias)
         xq, xs = o.quant_q8(xt)
-        for j in range(n_assign):
+        for j in range(min(n_assign, self.k)):
             e = self.experts[int(ids[0, j])]
             G, U = o.expert_gateup(xq[0], xs[0], e.wg, e.sg, e.wu, e.su)
             h = np.array([o.silu(g) * u for g, u in zip(G, U)], dtype=np.float32)
@@ -207,13 +218,13 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
-def oracle_rate(T, zipf, seconds):
+def oracle_rate(T, zipf, seconds, shared=False):
     """tokens/s of the oracle over ~`seconds` of CPU work (one core)."""
-    s = OracleSample(T, zipf)
+    s = OracleSample(T, zipf, shared=shared)
     s.run_assignments(1)  # warm
     done_tok, spent, i = 0.0, 0.0, 0
     while spent < seconds:
-        spent += s.run_assignments(s.k, i)
+        spent += s.run_assignments(s.units, i)
         done_tok += 1
         i += 1
     return done_tok / spent, f"{int(done_tok)} tokens of the {T}-token workload (whole layer per token, " \
@@ -226,26 +237,26 @@ def run_reference(args, rank, world):
     T, zipf, _ = WORKLOADS[args.workload]
     if rank != 0:
         return
-    s = OracleSample(T, zipf)
+    s = OracleSample(T, zipf, shared=args.shared_expert)
     t1 = s.run_assignments(1)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    m = int(max(1, min(s.k, budget // max(t1, 1e-6))))
+    m = int(max(1, min(s.units, budget // max(t1, 1e-6))))
     for i in range(args.warmup):
         s.run_assignments(m, i)
     tot = 0.0
     for i in range(args.steps):
         tot += s.run_assignments(m, i)
-    tok = args.steps * m / s.k
+    tok = args.steps * m / s.units
     value = tok / tot
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": args.workload, "tokens_per_step": T, "hidden": H, "experts": E, "top_k": K_TOP,
-                       "expert_intermediate": I_EXP},
+                       "expert_intermediate": I_EXP, "shared_expert": args.shared_expert},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: routing + {m} of the {s.k} expert slots of one token "
-                                       f"(tokens/s scaled by {m}/{s.k}); single-threaded C oracle"},
+                             "sample": f"each step: routing + {m} of the {s.units} expert passes of one token "
+                                       f"(tokens/s scaled by {m}/{s.units}); single-threaded C oracle"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -279,7 +290,7 @@ def main():
         NL = args.layers
     NX = 16 if T <= 64 else 2          # distinct token batches
     NG = NL * NX if T <= 64 else NL    # graphs: (layer copy, batch) pairs
-    layers = [make_layer(moe, torch, 1000 * rank + l, zipf, dev) for l in range(NL)]
+    layers = [make_layer(moe, torch, 1000 * rank + l, zipf, dev, shared=args.shared_expert) for l in range(NL)]
     gx = torch.Generator(device=dev)
     gx.manual_seed(7 + rank)
     xs = torch.randn(NX, T, H, generator=gx, device=dev).to(torch.bfloat16)
@@ -318,7 +329,7 @@ def main():
                 layer.forward(x, ws, stream)
             singles.append(g)
         for gj in range(NG // S):
-            ev = {stage: (mk_ev(), mk_ev())} if (in_graph_events and not fused) else None
+            ev = {stage: (mk_ev(), mk_ev())} if (in_graph_events and (not fused or args.shared_expert)) else None
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(S):
@@ -336,10 +347,13 @@ def main():
         uniq.append(int(torch.unique(ws.ids).numel()))
     A = T * K_TOP
     step_bytes = [ROUTER_BYTES + u * EXPERT_BYTES + T * H * 2 + T * H * 4 for u in uniq]
-    if fused:  # the one kernel moves the whole layer
-        gu_bytes = step_bytes
+    if fused:  # the one kernel moves the whole routed layer
+        gu_bytes = list(step_bytes)
     else:
         gu_bytes = [u * 2 * I_EXP * (H // 2 + H // 32) + T * (H + H // 32 * 4) + A * I_EXP * 4 for u in uniq]
+    if args.shared_expert:  # its weights, its Q8(x) and h rows, its output and the join
+        step_bytes = [b + EXPERT_BYTES + T * (H + H // 32 * 4) + T * I_EXP * 4 * 2 + T * H * 4 * 3
+                      for b in step_bytes]
 
     def run(n, start=0):
         """Steps start .. start+n-1: whole multi-step graphs where they line
@@ -378,13 +392,15 @@ def main():
         if dist:
             dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    if fused:
+    if fused and not args.shared_expert:
         # one launch per step: the kernel's average duration over the timed
         # region (launch gaps included, so an upper bound)
         gu_steps = list(range(K))
         gu_ms = [ms / K] * K
     elif in_graph_events:
-        # the gate/up launches of the first step of the last multi-step graphs replayed
+        # the dominant launches (gate/up, or the single-launch routed layer when
+        # a shared expert follows it) of the first step of the last multi-step
+        # graphs replayed
         firsts = [s for s in range(0, K - K % S, S)][-len(multis):]
         gu_steps = firsts
         gu_ms = [multi_events[(s % NG) // S][stage][0].elapsed_time(multi_events[(s % NG) // S][stage][1])
@@ -457,7 +473,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, sample = oracle_rate(T, zipf, args.cpu_seconds)
+        rate, sample = oracle_rate(T, zipf, args.cpu_seconds, shared=args.shared_expert)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
 
     if rank == 0:
@@ -471,7 +487,9 @@ def main():
                        "zipf_bias": zipf, "parallelism": f"replicas{world}",
                        "l2": f"{NL} layer copies x {NX} token batches cycled ({NL * 3.42:.1f} GB of weights > L2)",
                        "graph": f"CUDA graphs of {S} consecutive layer forwards (distinct layer copies), replayed back to back",
-                       "path": "fused single-launch decode" if fused else "six stage calls (8 kernels)",
+                       "path": ("fused single-launch decode" if fused else "six stage calls (8 kernels)")
+                               + (" + shared expert (stage calls + join)" if args.shared_expert else ""),
+                       "shared_expert": args.shared_expert,
                        "distinct_experts_mean": sum(uniq) / len(uniq)},
             "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,
             "roofline": roofline,
