@@ -312,6 +312,9 @@ def main():
     except TypeError:
         in_graph_events = False
     fused = moe.MoeLayer(layers[0]).use_fused(T)
+    # one launch per step (the shared expert, if any, inside it): its time is
+    # the timed region over the steps; else events bracket the dominant kernel
+    one_launch = fused and (not args.shared_expert or moe.MoeLayer(layers[0]).shared_in_one_launch(T))
     stage = "decode" if fused else "gateup"   # the dominant kernel
     S = args.graph_steps if (args.graph_steps > 1 and NG % args.graph_steps == 0) else 1
 
@@ -329,7 +332,7 @@ def main():
                 layer.forward(x, ws, stream)
             singles.append(g)
         for gj in range(NG // S):
-            ev = {stage: (mk_ev(), mk_ev())} if (in_graph_events and (not fused or args.shared_expert)) else None
+            ev = {stage: (mk_ev(), mk_ev())} if (in_graph_events and not one_launch) else None
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(S):
@@ -347,13 +350,15 @@ def main():
         uniq.append(int(torch.unique(ws.ids).numel()))
     A = T * K_TOP
     step_bytes = [ROUTER_BYTES + u * EXPERT_BYTES + T * H * 2 + T * H * 4 for u in uniq]
-    if fused:  # the one kernel moves the whole routed layer
+    routed_bytes = list(step_bytes)
+    if args.shared_expert:  # its weights, and its h and output rows
+        step_bytes = [b + EXPERT_BYTES + T * I_EXP * 4 * 2 + T * H * 4 * 2 for b in step_bytes]
+    if one_launch:  # the one kernel moves the whole layer (shared expert included)
         gu_bytes = list(step_bytes)
+    elif fused:  # the single launch moves the routed layer; the shared expert's calls follow
+        gu_bytes = routed_bytes
     else:
         gu_bytes = [u * 2 * I_EXP * (H // 2 + H // 32) + T * (H + H // 32 * 4) + A * I_EXP * 4 for u in uniq]
-    if args.shared_expert:  # its weights, its Q8(x) and h rows, its output and the join
-        step_bytes = [b + EXPERT_BYTES + T * (H + H // 32 * 4) + T * I_EXP * 4 * 2 + T * H * 4 * 3
-                      for b in step_bytes]
 
     def run(n, start=0):
         """Steps start .. start+n-1: whole multi-step graphs where they line
@@ -392,15 +397,15 @@ def main():
         if dist:
             dist.barrier()
     ms = ev0.elapsed_time(ev1)
-    if fused and not args.shared_expert:
+    if one_launch:
         # one launch per step: the kernel's average duration over the timed
         # region (launch gaps included, so an upper bound)
         gu_steps = list(range(K))
         gu_ms = [ms / K] * K
     elif in_graph_events:
-        # the dominant launches (gate/up, or the single-launch routed layer when
-        # a shared expert follows it) of the first step of the last multi-step
-        # graphs replayed
+        # the dominant launches (gate/up; or the routed single launch when the
+        # shared expert's calls follow it) of the first step of the last
+        # multi-step graphs replayed
         firsts = [s for s in range(0, K - K % S, S)][-len(multis):]
         gu_steps = firsts
         gu_ms = [multi_events[(s % NG) // S][stage][0].elapsed_time(multi_events[(s % NG) // S][stage][1])
@@ -488,7 +493,8 @@ def main():
                        "l2": f"{NL} layer copies x {NX} token batches cycled ({NL * 3.42:.1f} GB of weights > L2)",
                        "graph": f"CUDA graphs of {S} consecutive layer forwards (distinct layer copies), replayed back to back",
                        "path": ("fused single-launch decode" if fused else "six stage calls (8 kernels)")
-                               + (" + shared expert (stage calls + join)" if args.shared_expert else ""),
+                               + ("" if not args.shared_expert else " with the shared expert" if one_launch
+                                  else " + the shared expert's stage calls"),
                        "shared_expert": args.shared_expert,
                        "distinct_experts_mean": sum(uniq) / len(uniq)},
             "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,

@@ -269,6 +269,41 @@ MOE_API moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t 
                                       float *h, int64_t ld_h, float *y, int64_t ld_y,
                                       void *workspace, size_t ws_bytes, void *stream);
 
+/* Largest T that moe_decode_forward_shared accepts (its shared expert adds T
+ * rows to the single launch's shared memory and needs T*k <= 63). */
+MOE_API int moe_decode_max_tokens_shared(int H, int E, int k, int I);
+
+/* moe_decode_forward for a layer with a shared expert ("DeepSeek-V4-Flash on
+ * AMD gfx90a", Execution structure and Fig. 1), in the same single launch:
+ * the shared expert's gate/up slice is requested at the start (it does not
+ * depend on the routing) and computed while the router and top-k run; its
+ * down slice follows the routed ones; the combine then adds its output,
+ * out[t] = (routed combine)[t] + ys[t], fp32, so every output is bit-identical
+ * to moe_decode_forward followed by the shared expert's stage calls and
+ * moe_join_add.
+ *  shared_wg .. shared_sd  the shared expert's weights: one expert in the
+ *           routed experts' layout ([I][H/2], [I][H/32], [H][I/2], [H][I/32]);
+ *           16-byte aligned nibbles, 4-byte aligned scale bytes.
+ *  shared_h [T][ld_shared_h] fp32: its SwiGLU activations (output and
+ *           exchange buffer; 16-byte aligned, ld a multiple of 4).
+ *  shared_y [T][ld_shared_y] fp32: its down output, or NULL.
+ * Other arguments, requirements and errors as moe_decode_forward, with
+ * T <= moe_decode_max_tokens_shared(H, E, k, I). */
+MOE_API moe_status moe_decode_forward_shared(const void *x, moe_dtype x_dtype, int64_t ld_x,
+                                             const void *w_router, moe_dtype w_dtype, const float *bias,
+                                             const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
+                                             const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
+                                             const uint8_t *shared_wg, const uint8_t *shared_sg,
+                                             const uint8_t *shared_wu, const uint8_t *shared_su,
+                                             const uint8_t *shared_wd, const uint8_t *shared_sd,
+                                             int T, int H, int E, int k, int I,
+                                             float *out, int64_t ld_out,
+                                             float *logits, int32_t *ids, float *weights,
+                                             float *h, int64_t ld_h, float *y, int64_t ld_y,
+                                             float *shared_h, int64_t ld_shared_h,
+                                             float *shared_y, int64_t ld_shared_y,
+                                             void *workspace, size_t ws_bytes, void *stream);
+
 /* moe_decode_forward for callers that cannot allocate device memory when they
  * run the layer (serving loops that cannot afford the device-wide
  * synchronisation an allocation can cause, runtimes that own all device

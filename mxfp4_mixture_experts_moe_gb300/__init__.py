@@ -28,7 +28,8 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
            "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_join_add", "moe_decode_workspace_bytes",
-           "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc"]
+           "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc",
+           "moe_decode_max_tokens_shared", "moe_decode_forward_shared"]
 
 _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 _SIG = {
@@ -49,6 +50,9 @@ _SIG = {
     "moe_decode_forward": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L] + [_P] * 3
                            + [_P, _L, _P, _L, _P, C.c_size_t, _P]),
     "moe_decode_forward_noalloc": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L, _P]),
+    "moe_decode_max_tokens_shared": (_I, [_I, _I, _I, _I]),
+    "moe_decode_forward_shared": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 12 + [_I] * 5 + [_P, _L] + [_P] * 3
+                                  + [_P, _L, _P, _L, _P, _L, _P, _L, _P, C.c_size_t, _P]),
 }
 library_path = _LIB_PATH
 
@@ -208,6 +212,26 @@ def moe_decode_forward(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out, logits
                                    _ptr(out), _ld(out), _ptr(logits), _ptr(ids), _ptr(weights), _ptr(h), _ld(h),
                                    _ptr(y), _ld(y) if y is not None else 0, _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_decode_max_tokens_shared(H, E, k, I) -> int:
+    return _lib.moe_decode_max_tokens_shared(H, E, k, I)
+
+
+def moe_decode_forward_shared(x, w_router, bias, wg, sg, wu, su, wd, sd, shared, k, out, logits, ids, weights, h, y,
+                              shared_h, shared_y, workspace, stream=None):
+    """moe_decode_forward with the layer's shared expert (``shared`` has its
+    wg .. sd, one expert each) in the same launch."""
+    T, H = x.shape[0], w_router.shape[1]
+    E, I = w_router.shape[0], wg.shape[1]
+    _check(_lib.moe_decode_forward_shared(
+        _ptr(x), _dt(x), _ld(x), _ptr(w_router), _dt(w_router), _ptr(bias),
+        _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(wd), _ptr(sd),
+        _ptr(shared.wg), _ptr(shared.sg), _ptr(shared.wu), _ptr(shared.su), _ptr(shared.wd), _ptr(shared.sd),
+        T, H, E, k, I, _ptr(out), _ld(out), _ptr(logits), _ptr(ids), _ptr(weights), _ptr(h), _ld(h),
+        _ptr(y), _ld(y) if y is not None else 0, _ptr(shared_h), _ld(shared_h),
+        _ptr(shared_y), _ld(shared_y) if shared_y is not None else 0, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_decode_forward_noalloc(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out, stream=None):

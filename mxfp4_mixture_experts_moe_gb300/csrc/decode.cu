@@ -33,6 +33,7 @@ constexpr int kCons = kWarps - 1;  // warps 0..27 consume (<= 64 registers each)
 constexpr int kGroup = kCons / 2;  // consumer warps per ring item (two items in flight)
 constexpr int kMaxA = 64;          // assignments T*k handled by the fused path
 constexpr int kSlotWord = 8;       // first per-expert readiness word of the workspace
+constexpr int kSharedWord = kSlotWord + kMaxA - 1;  // the shared expert's (T*k <= kMaxA - 1 with one)
 
 struct DecodeArgs {
   const void *x;
@@ -67,26 +68,34 @@ struct DecodeArgs {
   int Rd;                 // max down rows per CTA (row stride of the y slice)
   int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
   int g16, d16;           // scale bytes copyable in 16-byte pieces
+  // optional shared expert: one more expert of the routed experts' format,
+  // run on every token with weight 1 and added after the routed combine
+  int shared;
+  const uint8_t *swg, *ssg, *swu, *ssu, *swd, *ssd;
+  float *sh_h;            // [T][ld_sh_h] its SwiGLU activations (exchange buffer)
+  int64_t ld_sh_h;
+  float *sh_y;            // [T][ld_sh_y] its down output, or null
+  int64_t ld_sh_y;
 };
 
 struct Misc {  // views into the small shared-memory region (A = T*k <= 64)
   int *ids;     // [A] expert of assignment a
   float *w;     // [A] routing weight of assignment a
-  int *srt;     // [A] assignment at sorted position p
+  int *srt;     // [R] assignment at sorted position p (R = A, + T shared-expert rows A + t)
   int *skey;    // [A] expert at sorted position p
-  int *segb;    // [A+1] start of the j-th expert segment (segb[nact] = A)
+  int *segb;    // [A+2] start of the j-th expert segment (segb[nact]: the routed rows; segb[nact+1]: + the shared expert's)
   int *active;  // [A] expert of the j-th segment, increasing id
   int *scalars; // [0] number of segments, [1] barrier flag, [2 + g] wait result of group g
 };
 
-MOE_DEVFN Misc misc_view(uint8_t *base, int A) {
+MOE_DEVFN Misc misc_view(uint8_t *base, int A, int R) {
   Misc m;
   int *p = reinterpret_cast<int *>(base);
   m.ids = p; p += A;
   m.w = reinterpret_cast<float *>(p); p += A;
-  m.srt = p; p += A;
+  m.srt = p; p += R;
   m.skey = p; p += A;
-  m.segb = p; p += A + 1;
+  m.segb = p; p += A + 2;
   m.active = p; p += A;
   m.scalars = p;
   return m;
@@ -356,7 +365,37 @@ MOE_DEVFN void rank_sort_warp(const Misc &m, int A, int E, unsigned *status) {
   }
 }
 
-template <int SG, int SD, bool FULL>
+// The producer warp's copies of one gate/up slice (rows row0 .. of both
+// matrices, Rg rows each) into the ring stage at sbase, completing on the
+// stage's full barrier fb (the whole warp calls it: the scale bytes may need
+// per-lane copies).
+MOE_DEVFN void gateup_copies(uint32_t sbase, uint32_t fb, const uint8_t *wg, const uint8_t *wu, const uint8_t *sg,
+                             const uint8_t *su, int64_t row0, uint32_t gwb, uint32_t gsb, const DecodeArgs &p, int H,
+                             int nbH, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(fb, 2 * gwb + (p.g16 ? 2 * gsb : 0u));
+    if (gwb > 0) {  // a CTA may own no gate/up rows when I < #SMs
+      bulk_g2s(sbase, wg + row0 * (H / 2), gwb, fb, pol);
+      bulk_g2s(sbase + p.gwreg, wu + row0 * (H / 2), gwb, fb, pol);
+      if (p.g16) {  // the slice's scale bytes are one contiguous 16-byte-aligned run
+        bulk_g2s(sbase + 2 * p.gwreg, sg + row0 * nbH, gsb, fb, pol);
+        bulk_g2s(sbase + 2 * p.gwreg + p.gsreg, su + row0 * nbH, gsb, fb, pol);
+      }
+    }
+  }
+  if (!p.g16) {
+#pragma unroll
+    for (int mm = 0; mm < 2; ++mm) {
+      const uint8_t *src = (mm == 0 ? sg : su) + row0 * nbH;
+      const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
+      for (uint32_t c = lane; c < gsb / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
+    }
+  }
+  cp_async_mbar_arrive_noinc(fb);
+}
+
+template <int SG, int SD, bool FULL, bool SHARED>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -374,11 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const uint32_t act = smem_addr(smem + p.off_act);
   float *yslice = reinterpret_cast<float *>(smem + p.off_y);
   float *logit_s = reinterpret_cast<float *>(smem + p.off_logit);
-  const Misc m = misc_view(smem + p.off_misc, A);
+  const Misc m = misc_view(smem + p.off_misc, A, A + (SHARED ? T : 0));
 
   const int nrw = (E + G - 1) / G;  // router warps in this kernel (host ensures <= 8)
   const uint32_t wsz = p.wbf ? 2u : 4u, xsz = p.xbf ? 2u : 4u;
-  const uint32_t front = smem_addr(smem);  // router rows, then x rows (the ring is not in use yet)
+  // router rows, then x rows, in ring stages not yet in use (stage 0 takes
+  // the shared expert's gate/up slice from the start)
+  constexpr int s0 = SHARED ? 1 : 0;  // gate/up ring items before the routed slots (the shared expert's)
+  const uint32_t front = smem_addr(smem) + (s0 ? p.stage_bytes : 0u);
   const uint32_t xs_smem = front + (uint32_t)nrw * H * wsz;
   uint64_t *fbar = full + 2 * nstage;
   if (tid == 0) {
@@ -412,7 +454,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     bar_base = v / (unsigned long long)G * (unsigned long long)G + hold;
   }
   __syncthreads();
-  if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(fbar), 0, p.status))) return;
+  // the shared expert does not depend on the routing: its gate/up slice is
+  // requested at once, into stage 0
+  if constexpr (SHARED) {
+    if (warp == kCons)
+      gateup_copies(smem_addr(smem), smem_addr(&full[0]), p.swg, p.swu, p.ssg, p.ssu, n0g, (uint32_t)Rg * (H / 2),
+                    (uint32_t)Rg * nbH, p, H, nbH, policy_evict_first());
+  }
+  // a CTA that gives up before the ring runs first lets that copy land
+  // (bounded), so no copy is still writing its shared memory when it exits
+  auto settle_shared = [&]() {
+    if (s0 && warp == kCons) mbar_wait(smem_addr(&full[0]), 0, p.status);
+  };
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(fbar), 0, p.status))) {
+    settle_shared();
+    return;
+  }
   const unsigned long long base = bar_base;
 
   // ---------------------------------------------------------------- A
@@ -441,7 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // CTA 0 clears the per-expert readiness words; barrier 1 publishes that
   // before any CTA can count on them
   if (cta == 0 && tid < kMaxA) p.bar[kSlotWord + tid] = 0ull;
-  if (!grid_barrier(p.bar, base + (unsigned long long)G, 0, kThreads, &m.scalars[1], p.status)) return;
+  if (!grid_barrier(p.bar, base + (unsigned long long)G, 0, kThreads, &m.scalars[1], p.status)) {
+    settle_shared();
+    return;
+  }
 
   // ---------------------------------------------------------------- A'
   for (int i = tid; i < T * E; i += kThreads) logit_s[i] = ldcg_f32(p.logits + i);
@@ -461,31 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const uint64_t pol = policy_evict_first();
   const uint32_t gwb = (uint32_t)Rg * (H / 2), gsb = (uint32_t)Rg * nbH;
   auto issue_gateup = [&](int st, int expert) {
-    const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
-    const uint32_t fb = smem_addr(&full[st]);
-    const int64_t row0 = (int64_t)expert * I + n0g;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(fb, 2 * gwb + (p.g16 ? 2 * gsb : 0u));
-      if (gwb > 0) {  // a CTA may own no gate/up rows when I < #SMs
-        bulk_g2s(sbase, p.wg + row0 * (H / 2), gwb, fb, pol);
-        bulk_g2s(sbase + p.gwreg, p.wu + row0 * (H / 2), gwb, fb, pol);
-        if (p.g16) {  // the slice's scale bytes are one contiguous 16-byte-aligned run
-          bulk_g2s(sbase + 2 * p.gwreg, p.sg + row0 * nbH, gsb, fb, pol);
-          bulk_g2s(sbase + 2 * p.gwreg + p.gsreg, p.su + row0 * nbH, gsb, fb, pol);
-        }
-      }
-    }
-    if (!p.g16) {
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        const uint8_t *src = (mm == 0 ? p.sg : p.su) + row0 * nbH;
-        const uint32_t dst = sbase + 2 * p.gwreg + mm * p.gsreg;
-        for (uint32_t c = lane; c < gsb / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
-      }
-    }
-    cp_async_mbar_arrive_noinc(fb);
+    gateup_copies(smem_addr(smem + (size_t)st * p.stage_bytes), smem_addr(&full[st]), p.wg, p.wu, p.sg, p.su,
+                  (int64_t)expert * I + n0g, gwb, gsb, p, H, nbH, pol);
   };
-  int early = 0;  // gate/up stages the producer already requested
+  int early = s0;  // gate/up ring items the producer already requested
   if (T == 1) {
     // one token: the producer warp merges, and requests slot j's gate/up slice
     // as soon as slot j is decided; the ring takes the slots in score order
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       int id[8];
       float wv[8];
       auto pick = [&](int j, int e) {
-        if (j < nstage && e >= 0 && e < E) issue_gateup(j, e);
+        if (j + s0 < nstage && e >= 0 && e < E) issue_gateup(j + s0, e);
       };
       topk_merge_stage(cand_key, cand_id, ngrp * k, k, id, wv, pick);
       bool valid = false;
@@ -526,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       }
     }
     __syncthreads();
-    early = min(nstage, m.scalars[0]);
+    early = min(nstage, s0 + m.scalars[0]);
   } else {
     if (warp < T) {
       int id[8];
@@ -553,7 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     }
   }
   const int nact = m.scalars[0];
-  const int ndi = p.dpp == 2 ? (nact + 1) >> 1 : (nact + p.dpp - 1) / p.dpp;  // down ring items (dpp slots each)
+  // ring items: the shared expert's gate/up (if any), the routed slots'
+  // gate/up, then the down items, dpp down slices each (the routed slots',
+  // then the shared expert's)
+  const int nslot = nact + s0;
+  const int ndi = p.dpp == 2 ? (nslot + 1) >> 1 : (nslot + p.dpp - 1) / p.dpp;
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
     // streams this CTA's gate/up slice of every active expert through the
@@ -561,42 +604,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     // are requested it asks for the down slices to be pulled into L2, so the
     // down copies (issued when gate/up stages free up) read from L2
     const uint32_t dw = (uint32_t)Rd * (I / 2), ds = (uint32_t)Rd * nbI;
-    const int first = nact < nstage ? nact : nstage;
+    const int first = nslot < nstage ? nslot : nstage;
+    // down slice j: a routed slot's expert (j < nact) or the shared expert
+    auto dsrc = [&](int j, const uint8_t *&w, const uint8_t *&sc) {
+      const bool shd = SHARED && j >= nact;
+      const int64_t drow0 = (int64_t)(shd ? 0 : m.active[j]) * H + n0d;
+      w = (shd ? p.swd : p.wd) + drow0 * (I / 2);
+      sc = (shd ? p.ssd : p.sd) + drow0 * nbI;
+    };
     // once the first stages are requested, pull the down slices into L2
     auto prefetch_down = [&]() {
       if (dw > 0) {
-        for (int j = lane; j < nact; j += 32) {
-          const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wd + drow0 * (I / 2)), "r"(dw) : "memory");
-          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.sd + drow0 * nbI), "r"(ds) : "memory");
+        for (int j = lane; j < nslot; j += 32) {
+          const uint8_t *w, *sc;
+          dsrc(j, w, sc);
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w), "r"(dw) : "memory");
+          if (p.d16) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(sc), "r"(ds) : "memory");
         }
       }
     };
     if (early >= first) prefetch_down();
     int issued = early;
-    for (int it = early; it < nact + ndi; ++it) {
+    for (int it = early; it < nslot + ndi; ++it) {
       const int st = it % nstage;
       if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
       const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
       const uint32_t fb = smem_addr(&full[st]);
-      if (it < nact) {
-        issue_gateup(st, m.active[it]);
+      if (it < nslot) {
+        issue_gateup(st, m.active[it - s0]);  // it >= early >= s0: the shared item went out at the start
       } else {
-        const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
+        const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, (uint32_t)(j1 - j0) * (dw + (p.d16 ? ds : 0u)));
           if (dw > 0) {
             for (int j = j0; j < j1; ++j) {
-              const int64_t drow0 = (int64_t)m.active[j] * H + n0d;
+              const uint8_t *w, *sc;
+              dsrc(j, w, sc);
               const uint32_t dst = sbase + (uint32_t)(j - j0) * p.dslot;
-              bulk_g2s(dst, p.wd + drow0 * (I / 2), dw, fb, pol);
-              if (p.d16) bulk_g2s(dst + p.dwreg, p.sd + drow0 * nbI, ds, fb, pol);
+              bulk_g2s(dst, w, dw, fb, pol);
+              if (p.d16) bulk_g2s(dst + p.dwreg, sc, ds, fb, pol);
             }
           }
         }
         if (!p.d16) {
           for (int j = j0; j < j1; ++j) {
-            const uint8_t *src = p.sd + ((int64_t)m.active[j] * H + n0d) * nbI;
+            const uint8_t *w, *src;
+            dsrc(j, w, src);
             const uint32_t dst = sbase + (uint32_t)(j - j0) * p.dslot + p.dwreg;
             for (uint32_t c = lane; c < ds / 4; c += 32) cp_async4(dst + 4 * c, src + 4 * c);
           }
@@ -626,12 +679,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const int grp = warp / kGroup, gw = warp - grp * kGroup;
   const int gbar = 3 + grp;  // named barrier of this group
   bool dead = false;
-  for (int it = grp; it < nact; it += 2) {
+  // the shared expert's item (ring item 0, landed long before the routed
+  // ones): every consumer warp, units of (row, token); its rows extend the
+  // sorted positions after the routed ones (srt = A + t), so the Q8(h) and
+  // down passes below treat it as one more segment
+  if (s0) {
+    if (warp == 0) {
+      const int nq0 = m.segb[nact];
+      for (int t = lane; t < T; t += 32) m.srt[nq0 + t] = A + t;
+      if (lane == 0) m.segb[nact + 1] = nq0 + T;
+    }
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[0]), 0, p.status));
+    if (!dead) {
+      const uint32_t sbase = smem_addr(smem);
+#pragma unroll 1
+      for (int u = warp; u < Rg * T; u += kCons) {
+        const int r = u / T, t = u - r * T;
+        const uint32_t wrow[2] = {sbase + (uint32_t)r * (H / 2), sbase + p.gwreg + (uint32_t)r * (H / 2)};
+        const uint32_t srow[2] = {sbase + 2 * p.gwreg + (uint32_t)r * nbH,
+                                  sbase + 2 * p.gwreg + p.gsreg + (uint32_t)r * nbH};
+        float acc[2];
+        row_dot_stage_pn<2, SG>(act + (uint32_t)t * p.xrow, H, wrow, srow, acc);
+        float g, u2;
+        reduce_pair(acc[0], acc[1], g, u2);
+        if (lane == 0) p.sh_h[(int64_t)t * p.ld_sh_h + n0g + r] = __fmul_rn(silu(g), u2);
+      }
+    }
+    bar_sync_named(1, kCons * 32);
+    if (warp == 0 && lane == 0)
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSharedWord), "l"(1ull) : "memory");
+    if (grp == 0 && lane == 0) mbar_arrive(smem_addr(&empty[0]));
+  }
+  for (int it = s0 + grp; it < nslot; it += 2) {
     const int st = it % nstage;
+    const int js = it - s0;  // routed slot
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
     if (!dead) {
-      const int sb = m.segb[it], se = m.segb[it + 1];
+      const int sb = m.segb[js], se = m.segb[js + 1];
 #pragma unroll 1
       for (int r = gw; r < Rg; r += kGroup) {
         const uint32_t wrow[2] = {sbase + (uint32_t)r * (H / 2), sbase + p.gwreg + (uint32_t)r * (H / 2)};
@@ -649,10 +734,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         }
       }
     }
-    // this CTA's h slice of expert slot it is written: count it (release)
+    // this CTA's h slice of expert slot js is written: count it (release)
     bar_sync_named(gbar, kGroup * 32);
     if (gw == 0 && lane == 0)
-      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSlotWord + it), "l"(1ull) : "memory");
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSlotWord + js), "l"(1ull) : "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
@@ -665,22 +750,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   if (warp == 0) {
     bool ok = m.scalars[4] == 0;
     for (int j = lane; j < nact; j += 32) ok = ok && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
+    if (s0 && lane == 0) ok = ok && wait_count(p.bar + kSharedWord, (unsigned long long)G, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0 && !ok) m.scalars[4] = 1;
   }
   bar_sync_named(1, kCons * 32);
   dead = m.scalars[4] != 0;  // one answer for the whole CTA from here on
   const uint32_t hq = smem_addr(smem + p.off_hq);  // Q8(h) rows by sorted position
-  const int nq = m.segb[nact];
+  const int nq = m.segb[nact];  // routed rows; the shared expert's T rows follow
   if (!dead) {
-    const int ntask = 2 * nq * nbI;  // (row, block, half), one per lane
+    const int ntask = 2 * (nq + s0 * T) * nbI;  // (row, block, half), one per lane
 #pragma unroll 1
     for (int c = warp; 32 * c < ntask; c += kCons) {
       const int idx = 32 * c + lane;
       const bool valid = idx < ntask;
       const int blk = valid ? idx >> 1 : 0;
       const int ql = blk / nbI, b = blk - ql * nbI;
-      const float *src = p.h + (int64_t)m.srt[ql] * p.ld_h + 32 * b + 16 * (idx & 1);
+      const float *src = ((SHARED && ql >= nq) ? p.sh_h + (int64_t)(ql - nq) * p.ld_sh_h
+                                               : p.h + (int64_t)m.srt[ql] * p.ld_h) + 32 * b + 16 * (idx & 1);
       float v[16];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -695,13 +782,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   }
   bar_sync_named(1, kCons * 32);
   // down ring items: every consumer warp takes every item; group g computes
-  // the item's slots g, g + 2, ... (a unit is two rows of one slot sharing
-  // the activation loads), then group 0 releases the stage
-  for (int it = nact; it < nact + ndi; ++it) {
+  // the item's slices g, g + 2, ... (a unit is two rows of one slice sharing
+  // the activation loads), then group 0 releases the stage.  Slice j < nact
+  // is routed slot j; slice nact the shared expert (its y rows follow the
+  // A routed ones in the slice buffer)
+  for (int it = nslot; it < nslot + ndi; ++it) {
     const int st = it % nstage;
     if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     if (!dead) {
-      const int j0 = (it - nact) * p.dpp, j1 = min(nact, j0 + p.dpp);
+      const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
       for (int j = j0 + grp; j < j1; j += 2) {
         const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes) + (uint32_t)(j - j0) * p.dslot;
         const int sb = m.segb[j], se = m.segb[j + 1];
@@ -719,11 +808,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
             float v0, v1;
             reduce_pair(acc[0], acc[1], v0, v1);
             if (lane == 0) {
+              const bool ys = SHARED && a >= A;  // the shared expert's row
+              float *yo = ys ? p.sh_y : p.y;      // optional global copies
+              const int64_t yrow = ys ? (int64_t)(a - A) * p.ld_sh_y : (int64_t)a * p.ld_y;
               yslice[a * p.Rd + r] = v0;
-              if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r] = v0;
+              if (yo) yo[yrow + n0d + r] = v0;
               if (two) {
                 yslice[a * p.Rd + r2] = v1;
-                if (p.y) p.y[(int64_t)a * p.ld_y + n0d + r2] = v1;
+                if (yo) yo[yrow + n0d + r2] = v1;
               }
             }
           }
@@ -740,29 +832,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     const float *wt = m.w + t * k;
     float acc = __fmul_rn(wt[0], yslice[(t * k) * p.Rd + r]);
     for (int j = 1; j < k; ++j) acc = __fmaf_rn(wt[j], yslice[(t * k + j) * p.Rd + r], acc);
+    if (s0) acc = __fadd_rn(acc, yslice[(A + t) * p.Rd + r]);  // the shared expert's join
     p.out[(int64_t)t * p.ld_out + n0d + r] = acc;
   }
 }
 
 using DecodeKernel = void (*)(DecodeArgs);
 
-DecodeKernel pick(int sg, int sd, bool full) {
-  if (full) {
-    if (sg == 4 && sd == 2) return decode_kernel<4, 2, true>;
-    if (sg == 4 && sd == 4) return decode_kernel<4, 4, true>;
-    if (sg == 2 && sd == 4) return decode_kernel<2, 4, true>;
-    if (sg == 2 && sd == 2) return decode_kernel<2, 2, true>;
+// The single-launch kernel for a shape.  With a shared expert, only the
+// DeepSeek-size shapes and the smallest one are instantiated (null otherwise).
+DecodeKernel pick(int sg, int sd, bool full, bool shared) {
+  if (shared) {
+    if (full && sg == 4 && sd == 2) return decode_kernel<4, 2, true, true>;
+    if (full && sg == 4 && sd == 4) return decode_kernel<4, 4, true, true>;
+    if (full && sg == 2 && sd == 4) return decode_kernel<2, 4, true, true>;
+    if (full && sg == 2 && sd == 2) return decode_kernel<2, 2, true, true>;
+    if (!full && sg == 1 && sd == 1) return decode_kernel<1, 1, false, true>;
+    return nullptr;
   }
-  if (sg == 1 && sd == 1) return decode_kernel<1, 1, false>;
-  if (sg == 2 && sd == 1) return decode_kernel<2, 1, false>;
-  if (sg == 2 && sd == 2) return decode_kernel<2, 2, false>;
-  if (sg == 4 && sd == 2) return decode_kernel<4, 2, false>;
-  if (sg == 4 && sd == 4) return decode_kernel<4, 4, false>;
-  if (sg == 1 && sd == 2) return decode_kernel<1, 2, false>;
-  if (sg == 2 && sd == 4) return decode_kernel<2, 4, false>;
-  if (sg == 4 && sd == 1) return decode_kernel<4, 1, false>;
-  if (sg == 1 && sd == 4) return decode_kernel<1, 4, false>;
+  if (full) {
+    if (sg == 4 && sd == 2) return decode_kernel<4, 2, true, false>;
+    if (sg == 4 && sd == 4) return decode_kernel<4, 4, true, false>;
+    if (sg == 2 && sd == 4) return decode_kernel<2, 4, true, false>;
+    if (sg == 2 && sd == 2) return decode_kernel<2, 2, true, false>;
+  }
+  if (sg == 1 && sd == 1) return decode_kernel<1, 1, false, false>;
+  if (sg == 2 && sd == 1) return decode_kernel<2, 1, false, false>;
+  if (sg == 2 && sd == 2) return decode_kernel<2, 2, false, false>;
+  if (sg == 4 && sd == 2) return decode_kernel<4, 2, false, false>;
+  if (sg == 4 && sd == 4) return decode_kernel<4, 4, false, false>;
+  if (sg == 1 && sd == 2) return decode_kernel<1, 2, false, false>;
+  if (sg == 2 && sd == 4) return decode_kernel<2, 4, false, false>;
+  if (sg == 4 && sd == 1) return decode_kernel<4, 1, false, false>;
+  if (sg == 1 && sd == 4) return decode_kernel<1, 4, false, false>;
   return nullptr;
+}
+
+// The kernel instantiation for H, I (K blocks per lane rounded up to 1, 2 or
+// 4), or null.
+DecodeKernel kernel_for(int H, int I, bool shared, int &SGp, int &SDp, bool &full) {
+  const int SG = (H / 32 + 31) / 32, SD = (I / 32 + 31) / 32;
+  SGp = SG == 3 ? 4 : SG;
+  SDp = SD == 3 ? 4 : SD;
+  full = H == 1024 * SGp && I == 1024 * SDp;
+  return pick(SGp, SDp, full, shared);
 }
 
 uint32_t align16(uint64_t v) { return (uint32_t)((v + 15) & ~uint64_t(15)); }
@@ -787,11 +900,12 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t act_bytes = align16((uint64_t)T * p.xrow);
   // Q8(h) of every assignment, in the region of Q8(x): the down phase
   // starts after every gate/up unit has read its activations
-  const uint64_t hq_bytes = align16((uint64_t)A * p.hrow);
-  const uint64_t y_bytes = align16((uint64_t)A * Rd * 4);
+  const int rows = A + (p.shared ? T : 0);  // h / y rows: the assignments, then the shared expert's tokens
+  const uint64_t hq_bytes = align16((uint64_t)rows * p.hrow);
+  const uint64_t y_bytes = align16((uint64_t)rows * Rd * 4);
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
   const uint64_t cand_bytes = (uint64_t)T * 8 * 8 * 8;  // top-k candidates: T x 8 groups x 8 (key, id)
-  const uint64_t misc_bytes = align16(4ull * (6 * A + 1 + 8));  // ids w srt skey segb active + 8 scalars
+  const uint64_t misc_bytes = align16(4ull * (5 * A + rows + 2 + 8));  // ids w srt skey segb active + 8 scalars
   const uint64_t tail = 16ull * 8 + std::max(act_bytes, hq_bytes) + y_bytes + logit_bytes + cand_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   if (tail >= budget) return false;
@@ -801,7 +915,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.nstage = ns;
   // the ring area first holds the CTA's router rows and the activation rows
   const uint64_t front = (uint64_t)((E + G - 1) / G) * H * (p.wbf ? 2 : 4) + (uint64_t)T * H * (p.xbf ? 2 : 4);
-  const uint64_t ring = std::max<uint64_t>((uint64_t)ns * p.stage_bytes, align16(front));
+  const uint64_t ring = std::max<uint64_t>((uint64_t)ns * p.stage_bytes,
+                                          (p.shared ? p.stage_bytes : 0) + align16(front));
   if (ring + tail > budget) return false;
   p.off_bars = (uint32_t)ring;
   p.off_act = p.off_bars + 16 * 8;
@@ -821,18 +936,24 @@ using namespace moe;
 
 extern "C" size_t moe_decode_workspace_bytes(void) { return 8 * (kSlotWord + kMaxA); }
 
-extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) {
+namespace {
+
+int max_tokens(int H, int E, int k, int I, bool shared) {
   if (H <= 0 || E <= 0 || k <= 0 || k > 8 || I <= 0 || H % 128 || I % 128 || H > 4096 || I > 4096 || E > 256) return 0;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
   const int G = sm_count();
   if ((E + G - 1) / G > 8) return 0;
+  int sgp = 0, sdp = 0;
+  bool full = false;
+  if (!kernel_for(H, I, shared, sgp, sdp, full)) return 0;
   int best = 0;
-  for (int T = 1; T <= kCons && T * k <= kMaxA; ++T) {
+  for (int T = 1; T <= kCons && T * k <= kMaxA - (shared ? 1 : 0); ++T) {
     DecodeArgs p{};
     p.T = T; p.H = H; p.E = E; p.k = k; p.I = I; p.A = T * k;
     p.wbf = 0; p.xbf = 0;  // fp32 router and activations: the larger staging
+    p.shared = shared;
     size_t smem = 0;
     if (plan_smem(p, G, optin, &smem)) best = T;
     else break;
@@ -840,13 +961,29 @@ extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) {
   return best;
 }
 
-extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
-                                         moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg,
-                                         const uint8_t *wu, const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
-                                         int T, int H, int E, int k, int I, float *out, int64_t ld_out,
-                                         float *logits, int32_t *ids, float *weights, float *h, int64_t ld_h,
-                                         float *y, int64_t ld_y, void *workspace, size_t ws_bytes, void *stream) {
-  const char *name = "moe_decode_forward";
+}  // namespace
+
+extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) { return max_tokens(H, E, k, I, false); }
+
+extern "C" int moe_decode_max_tokens_shared(int H, int E, int k, int I) { return max_tokens(H, E, k, I, true); }
+
+namespace {
+
+// The shared expert's arguments of moe_decode_forward_shared.
+struct SharedArgs {
+  const uint8_t *wg, *sg, *wu, *su, *wd, *sd;
+  float *h;
+  int64_t ld_h;
+  float *y;
+  int64_t ld_y;
+};
+
+moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
+                          moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
+                          const uint8_t *su, const uint8_t *wd, const uint8_t *sd, int T, int H, int E, int k, int I,
+                          float *out, int64_t ld_out, float *logits, int32_t *ids, float *weights, float *h,
+                          int64_t ld_h, float *y, int64_t ld_y, void *workspace, size_t ws_bytes,
+                          const SharedArgs *sh, void *stream) {
   if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: T=%d H=%d E=%d k=%d I=%d", name, T, H, E, k, I);
   if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad x dtype", name);
   if (w_dtype != MOE_F32 && w_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad router dtype", name);
@@ -857,6 +994,16 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   if (T == 0) return MOE_OK;
   const int A = T * k;
   if (A > kMaxA || T > kCons) return fail(MOE_ERR_UNSUPPORTED, "%s: T*k=%d beyond the fused decode path (<= %d)", name, A, kMaxA);
+  if (sh) {  // the shared expert's readiness word is the last one
+    if (A > kMaxA - 1) return fail(MOE_ERR_UNSUPPORTED, "%s: T*k=%d beyond the fused path with a shared expert (<= %d)", name, A, kMaxA - 1);
+    if (!sh->wg || !sh->sg || !sh->wu || !sh->su || !sh->wd || !sh->sd || !sh->h)
+      return fail(MOE_ERR_INVALID_ARG, "%s: null shared-expert pointer", name);
+    if ((uintptr_t)sh->wg % 16 || (uintptr_t)sh->wu % 16 || (uintptr_t)sh->wd % 16 || (uintptr_t)sh->sg % 4 ||
+        (uintptr_t)sh->su % 4 || (uintptr_t)sh->sd % 4)
+      return fail(MOE_ERR_INVALID_ARG, "%s: shared-expert weights must be 16-byte aligned, scale bytes 4-byte aligned", name);
+    if (sh->ld_h < I || sh->ld_h % 4 || (uintptr_t)sh->h % 16 || (sh->y && sh->ld_y < H))
+      return fail(MOE_ERR_INVALID_ARG, "%s: bad shared-expert output strides", name);
+  }
   if (!x || !w_router || !wg || !sg || !wu || !su || !wd || !sd || !out || !logits || !ids || !weights || !h || !workspace)
     return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", name);
   if (ws_bytes < moe_decode_workspace_bytes() || (uintptr_t)workspace % 8) return fail(MOE_ERR_INVALID_ARG, "%s: workspace too small", name);
@@ -876,10 +1023,9 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   const int G = sm_count();
   if ((E + G - 1) / G > 8) return fail(MOE_ERR_UNSUPPORTED, "%s: too many experts per SM", name);
   const int nbH = H / 32, nbI = I / 32;
-  const int SG = (nbH + 31) / 32, SD = (nbI + 31) / 32;
-  const int SGp = SG == 3 ? 4 : SG, SDp = SD == 3 ? 4 : SD;
-  const bool full = H == 1024 * SGp && I == 1024 * SDp;
-  DecodeKernel kern = pick(SGp, SDp, full);
+  int SGp = 0, SDp = 0;
+  bool full = false;
+  DecodeKernel kern = kernel_for(H, I, sh != nullptr, SGp, SDp, full);
   if (!kern) return fail(MOE_ERR_UNSUPPORTED, "%s: shape", name);
 
   DecodeArgs p{};
@@ -892,15 +1038,21 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   p.h = h; p.ld_h = ld_h; p.y = y; p.ld_y = ld_y;
   p.bar = static_cast<unsigned long long *>(workspace);
   p.status = device_status_word();
+  if (sh) {
+    p.shared = 1;
+    p.swg = sh->wg; p.ssg = sh->sg; p.swu = sh->wu; p.ssu = sh->su; p.swd = sh->wd; p.ssd = sh->sd;
+    p.sh_h = sh->h; p.ld_sh_h = sh->ld_h; p.sh_y = sh->y; p.ld_sh_y = sh->ld_y;
+  }
 
   size_t smem = 0;
   if (!plan_smem(p, G, optin, &smem)) return fail(MOE_ERR_UNSUPPORTED, "%s: T=%d does not fit the fused path's shared memory", name, T);
 
-  p.g16 = nbH % 16 == 0 && (uintptr_t)sg % 16 == 0 && (uintptr_t)su % 16 == 0;
-  p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0;
+  p.g16 = nbH % 16 == 0 && (uintptr_t)sg % 16 == 0 && (uintptr_t)su % 16 == 0 &&
+          (!sh || ((uintptr_t)sh->sg % 16 == 0 && (uintptr_t)sh->su % 16 == 0));
+  p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0 && (!sh || (uintptr_t)sh->sd % 16 == 0);
 
-  static bool configured[18][64] = {};
-  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2) + (full ? 9 : 0);
+  static bool configured[36][64] = {};
+  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2) + (full ? 9 : 0) + (sh ? 18 : 0);
   if (dev < 64 && !configured[ki][dev]) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
     if (err != cudaSuccess) return cuda_fail(err, name);
@@ -918,4 +1070,35 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
   cfg.numAttrs = 1;
   err = cudaLaunchKernelEx(&cfg, kern, p);
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
+}
+
+}  // namespace
+
+extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
+                                         moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg,
+                                         const uint8_t *wu, const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
+                                         int T, int H, int E, int k, int I, float *out, int64_t ld_out,
+                                         float *logits, int32_t *ids, float *weights, float *h, int64_t ld_h,
+                                         float *y, int64_t ld_y, void *workspace, size_t ws_bytes, void *stream) {
+  return decode_forward("moe_decode_forward", x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd, T, H,
+                        E, k, I, out, ld_out, logits, ids, weights, h, ld_h, y, ld_y, workspace, ws_bytes, nullptr,
+                        stream);
+}
+
+extern "C" moe_status moe_decode_forward_shared(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
+                                                moe_dtype w_dtype, const float *bias, const uint8_t *wg,
+                                                const uint8_t *sg, const uint8_t *wu, const uint8_t *su,
+                                                const uint8_t *wd, const uint8_t *sd, const uint8_t *shared_wg,
+                                                const uint8_t *shared_sg, const uint8_t *shared_wu,
+                                                const uint8_t *shared_su, const uint8_t *shared_wd,
+                                                const uint8_t *shared_sd, int T, int H, int E, int k, int I,
+                                                float *out, int64_t ld_out, float *logits, int32_t *ids,
+                                                float *weights, float *h, int64_t ld_h, float *y, int64_t ld_y,
+                                                float *shared_h, int64_t ld_shared_h, float *shared_y,
+                                                int64_t ld_shared_y, void *workspace, size_t ws_bytes, void *stream) {
+  const SharedArgs sh{shared_wg, shared_sg, shared_wu, shared_su, shared_wd, shared_sd,
+                      shared_h, ld_shared_h, shared_y, ld_shared_y};
+  return decode_forward("moe_decode_forward_shared", x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd,
+                        T, H, E, k, I, out, ld_out, logits, ids, weights, h, ld_h, y, ld_y, workspace, ws_bytes, &sh,
+                        stream);
 }

@@ -13,9 +13,9 @@ import dataclasses
 
 import torch
 
-from . import (act_quant_q8, moe_combine, moe_decode_forward, moe_decode_max_tokens, moe_decode_workspace_bytes,
-               moe_join_add, moe_mxfp4_down, moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens,
-               moe_sort_tokens_capacity)
+from . import (act_quant_q8, moe_combine, moe_decode_forward, moe_decode_forward_shared, moe_decode_max_tokens,
+               moe_decode_max_tokens_shared, moe_decode_workspace_bytes, moe_join_add, moe_mxfp4_down,
+               moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens, moe_sort_tokens_capacity)
 
 
 @dataclasses.dataclass
@@ -124,20 +124,31 @@ class MoeLayer:
         stage calls."""
         if self.fused is False:
             return False
+        self._limits()
+        return 0 < T <= self._max_t
+
+    def shared_in_one_launch(self, T: int) -> bool:
+        """A layer with a shared expert runs it inside the single launch for
+        batches up to moe_decode_max_tokens_shared(); between that and the
+        routed limit the shared expert follows as stage calls."""
+        return self.lw.shared is not None and self.use_fused(T) and T <= self._max_ts
+
+    def _limits(self):
         if not hasattr(self, "_max_t"):
             lw = self.lw
             self._max_t = moe_decode_max_tokens(lw.H, lw.E, lw.k, lw.I)
-        return 0 < T <= self._max_t
+            self._max_ts = 0 if lw.shared is None else moe_decode_max_tokens_shared(lw.H, lw.E, lw.k, lw.I)
 
     def forward(self, x: torch.Tensor, ws: Workspace, stream=None, events: dict | None = None) -> torch.Tensor:
         """out = MoE(x) for the T rows of x ([T, H] bf16/f32, unit column stride).
 
-        ``events`` optionally maps a stage name ("decode" for the single-launch
-        path; "route", "sort", "quant_x", "gateup", "quant_h", "down",
-        "combine" for the stage calls; "shared_quant_x", "shared_gateup",
-        "shared_quant_h", "shared_down", "join" for the shared expert) to a
-        (start, end) pair of torch.cuda.Event recorded around that stage on
-        ``stream``."""
+        ``events`` optionally maps a stage name ("decode" for the single launch,
+        with the shared expert when it fits; "route", "sort", "quant_x",
+        "gateup", "quant_h", "down", "combine" for the stage calls;
+        "shared_quant_x" (after the single launch only), "shared_gateup",
+        "shared_quant_h", "shared_down", "join" for the shared expert's stage
+        calls) to a (start, end) pair of torch.cuda.Event recorded around that
+        stage on ``stream``."""
         lw = self.lw
         s = torch.cuda.current_stream() if stream is None else stream
         ev = events or {}
@@ -149,14 +160,24 @@ class MoeLayer:
             if name in ev:
                 ev[name][1].record(s)
 
-        fused = self.use_fused(ws.T)
-        if fused:
+        sh = lw.shared
+        if self.use_fused(ws.T):
+            # one launch: the routed layer, and the shared expert when it fits
+            one = self.shared_in_one_launch(ws.T)
             if "decode" in ev:
                 ev["decode"][0].record(s)
-            moe_decode_forward(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, lw.k, ws.out, ws.logits,
-                               ws.ids, ws.w, ws.h, ws.y, ws.decode_ws, stream=s)
+            if one:
+                moe_decode_forward_shared(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, sh, lw.k,
+                                          ws.out, ws.logits, ws.ids, ws.w, ws.h, ws.y, ws.sh_h, ws.sh_y,
+                                          ws.decode_ws, stream=s)
+            else:
+                moe_decode_forward(x, lw.wr, lw.bias, lw.wg, lw.sg, lw.wu, lw.su, lw.wd, lw.sd, lw.k, ws.out,
+                                   ws.logits, ws.ids, ws.w, ws.h, ws.y, ws.decode_ws, stream=s)
             if "decode" in ev:
                 ev["decode"][1].record(s)
+            if one or sh is None:
+                return ws.out
+            stage("shared_quant_x", act_quant_q8, x, ws.xq, ws.xs)  # the single launch keeps Q8(x) on chip
         else:
             stage("route", moe_route_topk, x, lw.wr, lw.bias, lw.k, ws.logits, ws.ids, ws.w)
             stage("sort", moe_sort_tokens, ws.ids, lw.E, ws.tile_rows, ws.offsets, ws.sorted, ws.inv)
@@ -166,12 +187,9 @@ class MoeLayer:
             stage("quant_h", act_quant_q8, ws.h, ws.hq, ws.hs)
             stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
             stage("combine", moe_combine, ws.y, ws.w, ws.out)
-        sh = lw.shared
         if sh is not None:
             # the shared expert: the stage calls on its one-expert weight set
             # (every token, weight 1), then its join onto the routed output
-            if fused:
-                stage("shared_quant_x", act_quant_q8, x, ws.xq, ws.xs)
             stage("shared_gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, sh.wg, sh.sg, sh.wu, sh.su, ws.sh_offsets,
                   ws.sh_sorted, 1, ws.sh_h)
             stage("shared_quant_h", act_quant_q8, ws.sh_h, ws.sh_hq, ws.sh_hs)
@@ -182,7 +200,11 @@ class MoeLayer:
 
     def kernels_per_forward(self, T: int) -> int:
         """Launches of this library's kernels per forward."""
-        n = 1 if self.use_fused(T) else 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
+        if self.use_fused(T):
+            if self.lw.shared is None or self.shared_in_one_launch(T):
+                return 1
+            return 1 + 5  # the shared expert's quant x, gate/up, quant h, down, join
+        n = 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
         if self.lw.shared is not None:
-            n += 5 if self.use_fused(T) else 4  # (quant x), gate/up, quant h, down, join
+            n += 4  # the shared expert's gate/up, quant h, down, join
         return n

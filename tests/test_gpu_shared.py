@@ -3,11 +3,14 @@ and Fig. 1: a shared expert beside the routed experts, both feeding the join
 that adds their partials) against the oracle.
 
 The layer runs it as the stage calls on a one-expert weight set (every token,
-weight 1) followed by moe_join_add, after either the single-launch routed
-path or the routed stage calls.  Checked here:
+weight 1) followed by moe_join_add after the routed stage calls, or inside
+the single launch (moe_decode_forward_shared) for small batches.  Checked
+here:
 
 * the join: the joined output equals, bit for bit, the fp32 sum of the
   routed-only output and the shared expert's output;
+* the single launch against the stage calls: the same bits for the output,
+  the shared expert's h and its down output;
 * the shared expert's output against the oracle's, max|err| <= 1e-3 * RMS,
   plus the one-step Q8(h) allowance of the layer tests (a code of the
   GPU's h may sit one step from the oracle's where h * (1/scale) lies near a
@@ -69,23 +72,50 @@ def _run(moe, lw, x, T, fused):
     return ws, out
 
 
-@pytest.mark.parametrize("T,fused", [(1, True), (3, True), (3, False), (16, False), (20, False)])
-def test_shared_expert_tiny(moe, T, fused):
+def _check_fused_equals_stages(moe, lw, x, T):
+    """The single launch with the shared expert gives the stage calls' bits."""
+    assert moe.MoeLayer(lw).shared_in_one_launch(T)
+    ws_f = moe.Workspace(T, lw, "cuda")
+    out_f = host(moe.MoeLayer(lw, fused=True).forward(x, ws_f)).copy()
+    ws_s, out_s = _run(moe, lw, x, T, False)
+    assert bits_equal(out_f, out_s)
+    assert bits_equal(host(ws_f.sh_y), host(ws_s.sh_y))
+    assert bits_equal(host(ws_f.sh_h), host(ws_s.sh_h))
+    assert moe.moe_device_status() == 0
+    return ws_s
+
+
+def _run_mode(moe, lw, x, T, mode):
+    """mode "one": the single launch with the shared expert (checked against
+    the stage calls bit for bit); "mixed": the routed single launch, then the
+    shared expert's stage calls; "stages": stage calls for both."""
+    layer = moe.MoeLayer(lw)
+    if mode == "one":
+        return _check_fused_equals_stages(moe, lw, x, T)
+    if mode == "mixed":
+        if not layer.use_fused(T) or layer.shared_in_one_launch(T):
+            pytest.skip("this batch is not between the two single-launch limits")
+        return _run(moe, lw, x, T, True)[0]
+    return _run(moe, lw, x, T, False)[0]
+
+
+@pytest.mark.parametrize("T,mode", [(1, "one"), (3, "one"), (3, "stages"), (16, "stages"), (20, "stages")])
+def test_shared_expert_tiny(moe, T, mode):
     spec = synth.TINY
     sh, lw = _with_shared(upload_layer(spec), spec)
     x = synth.activations(spec, T)
-    ws, out = _run(moe, lw, dev(x), T, fused)
+    ws = _run_mode(moe, lw, dev(x), T, mode)
     xq, xs = oracle.quant_q8(x)
     _check_shared_output(ws, oracle.shared_expert(xq, xs, sh))
 
 
-@pytest.mark.parametrize("T,fused", [(1, True), (8, False), (24, False)])
-def test_shared_expert_dsv4(moe, T, fused):
+@pytest.mark.parametrize("T,mode", [(1, "one"), (3, "one"), (4, "mixed"), (8, "stages"), (24, "stages")])
+def test_shared_expert_dsv4(moe, T, mode):
     spec = synth.DSV4
     x = synth.activations(spec, T, token0=40)
     _, ids, _ = oracle.route(x, synth.router_weights(spec), spec.k)
     sh, lw = _with_shared(upload_layer(spec, only=set(ids.ravel().tolist())), spec)
-    ws, out = _run(moe, lw, dev(x), T, fused)
+    ws = _run_mode(moe, lw, dev(x), T, mode)
     xq, xs = oracle.quant_q8(x)
     _check_shared_output(ws, oracle.shared_expert(xq, xs, sh))
 
