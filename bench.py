@@ -60,6 +60,7 @@ METRIC = "MoE-layer tokens/s and achieved HBM TB/s (decode 1–16 rows; prefill 
 # copy of the workload; workloads without a capture report null.
 NCU_TRAFFIC = {
     ("decode-1", "moe_decode_forward"): 83.88e6,
+    ("decode-1", "moe_decode_forward_shared"): 98.0e6,
     ("prefill-512", "moe_mxfp4_gateup_swiglu"): 2.3209e9,
 }
 
@@ -468,7 +469,8 @@ def main():
     if gu_ms:
         gb = sum(gu_bytes[s % NG] for s in gu_steps)
         achieved = gb / (sum(gu_ms) * 1e-3) / 1e9
-        rk = "moe_decode_forward" if fused else "moe_mxfp4_gateup_swiglu"
+        rk = ("moe_decode_forward_shared" if one_launch and args.shared_expert else "moe_decode_forward") if fused \
+            else "moe_mxfp4_gateup_swiglu"
         roofline = {"kernel": rk, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get((args.workload, rk)),
                     "peak_kind": peak_kind, "launches_timed": len(gu_ms),
