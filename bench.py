@@ -264,6 +264,17 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(dist, seconds: float) -> float:
+    """The largest of the ranks' times (every rank gets it); the value itself
+    without a process group."""
+    if not dist:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -413,10 +424,7 @@ def main():
                  for s in firsts]
     else:
         gu_steps, gu_ms = [], []
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, ms)
     ms_step = ms / K
     bytes_mean = sum(step_bytes[s % NG] for s in range(K)) / K
     value = world * T * K / (ms * 1e-3)
@@ -453,10 +461,7 @@ def main():
                 outh.copy_(ws.out, non_blocking=True)
                 stream.synchronize()
             e2e_s = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([e2e_s], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(dist, e2e_s)
         e2e_value = world * T * Ke / e2e_s
 
         e2e = {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
