@@ -86,9 +86,11 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 /* Message for the last non-OK status returned on this host thread. */
 MOE_API const char *moe_last_error(void);
 
-/* ABI version of this header (bumped on any signature change). */
+/* ABI version of this header (bumped on any signature change or addition;
+ * 2 adds moe_join_add, moe_decode_max_tokens_shared and
+ * moe_decode_forward_shared). */
 MOE_API int moe_abi_version(void);
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device into *flags (may be NULL).  Returns MOE_ERR_DEVICE when the

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in _declared():
         assert hasattr(lib, n), n
     assert set(moe.EXPORTS) == _declared()
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 def test_library_exports_nothing_else():
