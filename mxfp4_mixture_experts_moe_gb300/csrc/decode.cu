@@ -68,6 +68,7 @@ struct DecodeArgs {
   int Rd;                 // max down rows per CTA (row stride of the y slice)
   int Rg;                 // max gate/up rows per CTA (row stride of the gate/up sums)
   int g16, d16;           // scale bytes copyable in 16-byte pieces
+  int hqr;                // Q8(h) in the last ring stage during the down phase (down items skip that stage)
   // optional shared expert: one more expert of the routed experts' format,
   // run on every token with weight 1 and added after the routed combine
   int shared;
@@ -219,8 +220,9 @@ MOE_DEVFN float router_dot_smem(uint32_t wrow, bool wbf, uint32_t xrow, bool xbf
   return p;
 }
 
-// Q8 of one 32-value block into a staged row (split-half layout with the
-// scale and the exact block sum), optionally also to global codes/scales.
+// Q8 of one 32-value block into a staged row: codes in the split-half layout
+// (elements 0..15 of block b at 16 b, 16..31 at 16 (nb + b)), then the
+// block scales.
 MOE_DEVFN void q8_to_row(const float (&v)[32], uint32_t row, int K, int b) {
   const int nb = K / 32;
   uint32_t pk[8];
@@ -229,15 +231,14 @@ MOE_DEVFN void q8_to_row(const float (&v)[32], uint32_t row, int K, int b) {
   sts128(row + 16u * b, make_uint4(pk[0], pk[1], pk[2], pk[3]));
   sts128(row + 16u * (nb + b), make_uint4(pk[4], pk[5], pk[6], pk[7]));
   sts32(row + (uint32_t)K + 4u * b, __float_as_uint(d));
-  sts32(row + (uint32_t)K + 4u * (nb + b), (uint32_t)sum);
 }
 
 // Q8 of one 32-value block by a lane pair (lanes 2i, 2i+1; the whole warp
 // must call): each lane holds 16 values (half 0: elements 0..15, half 1:
-// 16..31).  amax and the code sum are combined across the pair; every other
-// step is q8_block's, element by element, so the codes, scale and sum are
-// q8_block's.  Half 0 writes the first half-block plane, the scale and the
-// sum; half 1 the second plane.
+// 16..31).  amax is combined across the pair; every other step is
+// q8_block's, element by element, so the codes and the scale are q8_block's.
+// Half 0 writes the first half-block plane and the scale, half 1 the second
+// plane.
 MOE_DEVFN void q8_pair_to_row(const float (&v)[16], int half, bool store, uint32_t row, int K, int b) {
   const int nb = K / 32;
   float amax = 0.0f;
@@ -247,7 +248,6 @@ MOE_DEVFN void q8_pair_to_row(const float (&v)[16], int half, bool store, uint32
   const float d = __fdiv_rn(amax, 127.0f);
   const float inv = d > 0.0f ? __frcp_rn(d) : 0.0f;
   uint32_t pk[4];
-  int sum = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t word = 0;
@@ -255,18 +255,13 @@ MOE_DEVFN void q8_pair_to_row(const float (&v)[16], int half, bool store, uint32
     for (int j = 0; j < 4; ++j) {
       int qi = __float2int_rn(__fmul_rn(v[4 * c + j], inv));
       qi = max(-127, min(127, qi));
-      sum += qi;
       word |= (uint32_t)(qi & 0xFF) << (8 * j);
     }
     pk[c] = word;
   }
-  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
   if (store) {
     sts128(row + 16u * (half ? nb + b : b), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-    if (half == 0) {
-      sts32(row + (uint32_t)K + 4u * b, __float_as_uint(d));
-      sts32(row + (uint32_t)K + 4u * (nb + b), (uint32_t)sum);
-    }
+    if (half == 0) sts32(row + (uint32_t)K + 4u * b, __float_as_uint(d));
   }
 }
 
@@ -363,6 +358,21 @@ MOE_DEVFN void rank_sort_warp(const Misc &m, int A, int E, unsigned *status) {
     m.segb[__popc(bal)] = nvalid;
     m.scalars[0] = __popc(bal);
   }
+}
+
+// Ring stage of item it, and how many earlier items used that stage (the
+// phase parity of its barriers).  Gate/up items cycle through the NS stages;
+// with hqr the down items cycle through the first NS - 1, the last one
+// holding Q8(h) during the down phase.
+MOE_DEVFN void ring_slot(int it, int nslot, int NS, bool hqr, int &st, int &use) {
+  if (!hqr || it < nslot) {
+    st = it % NS;
+    use = it / NS;
+    return;
+  }
+  const int d = it - nslot, NSd = NS - 1;
+  st = d % NSd;
+  use = (nslot - st + NS - 1) / NS + d / NSd;  // gate/up items on stage st, then earlier down items
 }
 
 // The producer warp's copies of one gate/up slice (rows row0 .. of both
@@ -626,8 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     if (early >= first) prefetch_down();
     int issued = early;
     for (int it = early; it < nslot + ndi; ++it) {
-      const int st = it % nstage;
-      if (it >= nstage && !mbar_wait(smem_addr(&empty[st]), ((it / nstage) - 1) & 1, p.status)) break;
+      int st, use;
+      ring_slot(it, nslot, nstage, p.hqr, st, use);
+      if (use >= 1 && !mbar_wait(smem_addr(&empty[st]), (use - 1) & 1, p.status)) break;
       const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
       const uint32_t fb = smem_addr(&full[st]);
       if (it < nslot) {
@@ -659,8 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       issued = it + 1;
       if (it == first - 1) prefetch_down();
     }
-    for (int it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
-      mbar_wait(smem_addr(&full[it % nstage]), (it / nstage) & 1, p.status);
+    // before exiting, the latest copy into every stage has landed
+    uint32_t seen = 0;
+    for (int it = issued - 1; it >= 0 && it >= issued - 2 * nstage; --it) {
+      int st, use;
+      ring_slot(it, nslot, nstage, p.hqr, st, use);
+      if ((seen >> st) & 1u) continue;
+      seen |= 1u << st;
+      mbar_wait(smem_addr(&full[st]), use & 1, p.status);
+    }
     return;
   }
 
@@ -756,7 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   }
   bar_sync_named(1, kCons * 32);
   dead = m.scalars[4] != 0;  // one answer for the whole CTA from here on
-  const uint32_t hq = smem_addr(smem + p.off_hq);  // Q8(h) rows by sorted position
+  // Q8(h) rows by sorted position: the last ring stage (idle once every
+  // gate/up item is consumed; the down items skip it) or the region of Q8(x)
+  const uint32_t hq = smem_addr(smem + (p.hqr ? (size_t)(nstage - 1) * p.stage_bytes : (size_t)p.off_hq));
   const int nq = m.segb[nact];  // routed rows; the shared expert's T rows follow
   if (!dead) {
     const int ntask = 2 * (nq + s0 * T) * nbI;  // (row, block, half), one per lane
@@ -787,8 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // is routed slot j; slice nact the shared expert (its y rows follow the
   // A routed ones in the slice buffer)
   for (int it = nslot; it < nslot + ndi; ++it) {
-    const int st = it % nstage;
-    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
+    int st, use;
+    ring_slot(it, nslot, nstage, p.hqr, st, use);
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), use & 1, p.status));
     if (!dead) {
       const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
       for (int j = j0 + grp; j < j1; j += 2) {
@@ -895,8 +916,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.dslot = (dstage + 127u) & ~127u;
   p.stage_bytes = ((gstage > p.dslot ? gstage : p.dslot) + 127u) & ~127u;
   p.dpp = (int)(p.stage_bytes / p.dslot);
-  p.xrow = (uint32_t)H + 8u * nbH;
-  p.hrow = (uint32_t)I + 8u * nbI;
+  p.xrow = (uint32_t)H + 4u * nbH;  // codes, then the block scales
+  p.hrow = (uint32_t)I + 4u * nbI;
   const uint64_t act_bytes = align16((uint64_t)T * p.xrow);
   // Q8(h) of every assignment, in the region of Q8(x): the down phase
   // starts after every gate/up unit has read its activations
@@ -906,11 +927,16 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
   const uint64_t cand_bytes = (uint64_t)T * 8 * 8 * 8;  // top-k candidates: T x 8 groups x 8 (key, id)
   const uint64_t misc_bytes = align16(4ull * (5 * A + rows + 2 + 8));  // ids w srt skey segb active + 8 scalars
-  const uint64_t tail = 16ull * 8 + std::max(act_bytes, hq_bytes) + y_bytes + logit_bytes + cand_bytes + misc_bytes;
+  const uint64_t small = 16ull * 8 + y_bytes + logit_bytes + cand_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
-  if (tail >= budget) return false;
-  int ns = (int)((budget - tail) / p.stage_bytes);
-  if (ns > 4) ns = 4;
+  auto stages = [&](uint64_t tail) { return tail >= budget ? 0 : std::min<int>(4, (int)((budget - tail) / p.stage_bytes)); };
+  // Q8(h) in the region of Q8(x) (both outside the ring), or in the last
+  // ring stage during the down phase when that gives the ring one more stage
+  // (the down items then cycle through one stage fewer)
+  const int ns_apart = stages(small + std::max(act_bytes, hq_bytes)), ns_in = stages(small + act_bytes);
+  p.hqr = hq_bytes <= p.stage_bytes && ns_in >= 3 && ns_in > ns_apart;
+  const uint64_t tail = small + (p.hqr ? act_bytes : std::max(act_bytes, hq_bytes));
+  const int ns = p.hqr ? ns_in : ns_apart;
   if (ns < 2) return false;
   p.nstage = ns;
   // the ring area first holds the CTA's router rows and the activation rows
@@ -921,7 +947,7 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   p.off_bars = (uint32_t)ring;
   p.off_act = p.off_bars + 16 * 8;
   p.off_hq = p.off_act;
-  p.off_y = p.off_act + (uint32_t)std::max(act_bytes, hq_bytes);
+  p.off_y = p.off_act + (uint32_t)(p.hqr ? act_bytes : std::max(act_bytes, hq_bytes));
   p.off_logit = p.off_y + (uint32_t)y_bytes;
   p.off_cand = p.off_logit + (uint32_t)logit_bytes;
   p.off_misc = p.off_cand + (uint32_t)cand_bytes;
