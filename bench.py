@@ -59,8 +59,8 @@ METRIC = "MoE-layer tokens/s and achieved HBM TB/s (decode 1–16 rows; prefill 
 # roofline kernel, from one ncu capture of the current kernels on a one-layer
 # copy of the workload; workloads without a capture report null.
 NCU_TRAFFIC = {
-    ("decode-1", "moe_decode_forward"): 83.88e6,
-    ("decode-1", "moe_decode_forward_shared"): 98.0e6,
+    ("decode-1", "moe_decode_forward"): 84.02e6,
+    ("decode-1", "moe_decode_forward_shared"): 98.02e6,
     ("prefill-512", "moe_mxfp4_gateup_swiglu"): 2.3209e9,
 }
 
