@@ -319,11 +319,14 @@ MOE_API moe_status moe_decode_forward_shared(const void *x, moe_dtype x_dtype, i
  * Limits of that array: T*k <= 64, T*E <= 32768, I <= 4096; beyond them the
  * call returns MOE_ERR_UNSUPPORTED (use moe_decode_forward with your own
  * buffers).
- * The first call on a device looks up the array's device address (set-up);
- * make that first call before any stream capture.  Each call clears the
- * barrier words on `stream` before its launch.  All calls on one device share
- * the array: calls that may overlap on the GPU (different streams without
- * ordering between them) race and give wrong results. */
+ * Every call looks up the array's device address on the current device (a
+ * host-side query); the first call on a device also loads the library's
+ * module there, so make that first call before any stream capture.  Each call
+ * checks every argument first and, only then, clears the barrier words on
+ * `stream` before its launch (a rejected call enqueues nothing).  All calls
+ * on one device share the array: calls that may overlap on the GPU
+ * (different streams without ordering between them) race and give wrong
+ * results. */
 MOE_API moe_status moe_decode_forward_noalloc(const void *x, moe_dtype x_dtype, int64_t ld_x,
                                               const void *w_router, moe_dtype w_dtype, const float *bias,
                                               const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,

@@ -1,7 +1,13 @@
 // Host side of the C ABI: error reporting, the device status word, device
-// properties.
+// properties, and the one-time kernel attributes.  The per-device caches are
+// filled under a mutex, so host threads may make their first calls at once.
 #include <stdarg.h>
 #include <stdio.h>
+
+#include <map>
+#include <mutex>
+#include <set>
+#include <tuple>
 
 #include "common.cuh"
 
@@ -13,13 +19,36 @@ thread_local char g_last_error[512] = "";
 // reads and clears it.  One word per device (a module-scope device variable).
 __device__ unsigned g_device_status = 0;
 
-unsigned *g_status_ptr[64] = {nullptr};
-int g_sm_count[64] = {0};
+struct DeviceInfo {
+  unsigned *status = nullptr;  // device address of g_device_status
+  int sms = 0;
+};
+
+std::mutex g_info_mu;
+std::map<int, DeviceInfo> g_info;                        // by device ordinal
+std::set<std::tuple<const void *, int, int>> g_attr_set;  // (kernel, device, bytes) already configured
 
 int current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   return dev;
+}
+
+// The current device's cached properties (filled on first use), or null.
+const DeviceInfo *device_info() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_info_mu);
+  DeviceInfo &d = g_info[dev];
+  if (!d.status) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return nullptr;
+    d.sms = n;
+    d.status = static_cast<unsigned *>(p);
+  }
+  return &d;
 }
 
 }  // namespace
@@ -39,25 +68,25 @@ moe_status cuda_fail(cudaError_t e, const char *what) {
 }
 
 unsigned *device_status_word() {
-  const int dev = current_device();
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!g_status_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<unsigned *>(p);
-  }
-  return g_status_ptr[dev];
+  const DeviceInfo *d = device_info();
+  return d ? d->status : nullptr;
 }
 
 int sm_count() {
+  const DeviceInfo *d = device_info();
+  return d ? d->sms : 1;
+}
+
+moe_status ensure_smem_attr(const void *kern, int bytes, const char *name) {
   const int dev = current_device();
-  if (dev < 0 || dev >= 64) return 1;
-  if (!g_sm_count[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    g_sm_count[dev] = n;
-  }
-  return g_sm_count[dev];
+  if (dev < 0) return fail(MOE_ERR_CUDA, "%s: no current CUDA device", name);
+  std::lock_guard<std::mutex> lock(g_info_mu);
+  const auto key = std::make_tuple(kern, dev, bytes);
+  if (g_attr_set.count(key)) return MOE_OK;
+  const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err != cudaSuccess) return cuda_fail(err, name);
+  g_attr_set.insert(key);
+  return MOE_OK;
 }
 
 }  // namespace moe

@@ -18,6 +18,9 @@ moe_status fail(moe_status s, const char *fmt, ...);
 moe_status cuda_fail(cudaError_t e, const char *what);
 unsigned *device_status_word();  // per-device address of the status word, or NULL
 int sm_count();
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes) on the current
+// device, once per (kernel, device, bytes); thread-safe.
+moe_status ensure_smem_attr(const void *kern, int bytes, const char *name);
 
 // Tensor-core path of the expert projections (tc_expert.cu): mode 0 gate/up
 // with SwiGLU into out0, 1 gate into out0 and up into out1, 2 down into out0.
@@ -29,6 +32,24 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
                             const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
                             int K, int N, int bytoken, float *out0, float *out1, int64_t ld_out, cudaStream_t stream,
                             const char *name);
+
+// The single-launch decode forward (decode.cu) behind moe_decode_forward and
+// moe_decode_forward_shared: their arguments, the shared expert's (sh, or
+// null), and clear_ws: zero the workspace on the stream right before the
+// launch, once every argument check has passed.
+struct SharedArgs {
+  const uint8_t *wg, *sg, *wu, *su, *wd, *sd;
+  float *h;
+  int64_t ld_h;
+  float *y;
+  int64_t ld_y;
+};
+moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
+                          moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
+                          const uint8_t *su, const uint8_t *wd, const uint8_t *sd, int T, int H, int E, int k, int I,
+                          float *out, int64_t ld_out, float *logits, int32_t *ids, float *weights, float *h,
+                          int64_t ld_h, float *y, int64_t ld_y, void *workspace, size_t ws_bytes,
+                          const SharedArgs *sh, bool clear_ws, void *stream);
 
 // Token of assignment a = t*k + j, i.e. a / k, as a multiply-high by
 // kdiv_of(k) = ceil(2^32 / k), exact for a < 2^28 and k <= 8.  k = 1 is

@@ -54,7 +54,8 @@ struct DecodeArgs {
   int64_t ld_h;
   float *y;  // optional
   int64_t ld_y;
-  unsigned long long *bar;  // [0] arrival counter, [1] hold (0), [kSlotWord + j] h of expert slot j done
+  unsigned long long *bar;  // [0] arrival counter, [1] barrier hold (0), [2] readiness hold (0),
+                            // [kSlotWord + j] h of expert slot j done
   unsigned *status;
   // geometry (host-computed)
   int nstage;
@@ -441,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
     mbar_init(smem_addr(fbar), 1);
     fence_mbar_init();
     m.scalars[4] = 0;
+    m.scalars[5] = 0;
     // stage this CTA's router rows and the T activation rows with bulk copies
     int nrows = 0;
     for (int w = 0; w < nrw; ++w) nrows += (cta + G * w) < E;
@@ -456,12 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       bulk_g2s(xs_smem + (uint32_t)t * H * xsz, static_cast<const uint8_t *>(p.x) + (int64_t)t * p.ld_x * xsz, H * xsz,
                smem_addr(fbar), pol);
   }
-  __shared__ unsigned long long bar_base;
+  __shared__ unsigned long long bar_base, ready_hold;
   if (tid == 32) {
-    unsigned long long v, hold;
+    unsigned long long v, hold, rhold;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(hold) : "l"(p.bar + 1) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(rhold) : "l"(p.bar + 2) : "memory");
     bar_base = v / (unsigned long long)G * (unsigned long long)G + hold;
+    ready_hold = rhold;  // 0 in use; a test sets it to make the readiness waits run out
   }
   __syncthreads();
   // the shared expert does not depend on the routing: its gate/up slice is
@@ -670,14 +674,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       issued = it + 1;
       if (it == first - 1) prefetch_down();
     }
-    // before exiting, the latest copy into every stage has landed
-    uint32_t seen = 0;
-    for (int it = issued - 1; it >= 0 && it >= issued - 2 * nstage; --it) {
+    // before exiting, the latest copy into every stage has landed: the last
+    // item issued into each stage (1 + its use count, 16 bits per stage; with
+    // hqr the down items skip the last stage, so its latest copy can be a
+    // gate/up item long before the end)
+    uint64_t last = 0;
+    for (int it = 0; it < issued; ++it) {
       int st, use;
       ring_slot(it, nslot, nstage, p.hqr, st, use);
-      if ((seen >> st) & 1u) continue;
-      seen |= 1u << st;
-      mbar_wait(smem_addr(&full[st]), use & 1, p.status);
+      last = (last & ~(0xFFFFull << (16 * st))) | ((uint64_t)(use + 1) << (16 * st));
+    }
+    for (int st = 0; st < nstage; ++st) {
+      const int u1 = (int)((last >> (16 * st)) & 0xFFFFu);
+      if (u1) mbar_wait(smem_addr(&full[st]), (u1 - 1) & 1, p.status);
     }
     return;
   }
@@ -692,8 +701,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // quantise every h row into shared memory at once (the region of Q8(x),
   // no longer read), then the groups take the down ring items (dpp slots
   // each, their slices already pulled into L2) in units of two rows of one
-  // slot, and leave y in shared memory for the combine.  A warp whose wait gave up stops computing but keeps arriving
-  // on the ring and on the named barriers, so no other warp waits on it.
+  // slot, and leave y in shared memory for the combine.  A warp whose wait
+  // gave up stops computing but keeps arriving on the ring and on the named
+  // barriers, so no other warp waits on it.  It still waits (bounded) for
+  // each ring copy to land before it releases the stage, so the producer
+  // never re-arms a stage with a copy in flight, unless a copy itself never
+  // landed ("broken"): then it stops waiting on the ring.
   const int grp = warp / kGroup, gw = warp - grp * kGroup;
   const int gbar = 3 + grp;  // named barrier of this group
   bool dead = false;
@@ -763,17 +776,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // ---- down phase
   // once every slot is complete in every CTA (one warp polls the readiness
   // words), all consumer warps quantise every h row into shared memory
-  if (dead && lane == 0) m.scalars[4] = 1;
+  if (dead && lane == 0) {  // in the gate/up phase only a ring copy that never landed makes a warp give up
+    m.scalars[4] = 1;
+    m.scalars[5] = 1;
+  }
   bar_sync_named(1, kCons * 32);
   if (warp == 0) {
     bool ok = m.scalars[4] == 0;
-    for (int j = lane; j < nact; j += 32) ok = ok && wait_count(p.bar + kSlotWord + j, (unsigned long long)G, p.status);
-    if (s0 && lane == 0) ok = ok && wait_count(p.bar + kSharedWord, (unsigned long long)G, p.status);
+    const unsigned long long ready = (unsigned long long)G + ready_hold;
+    for (int j = lane; j < nact; j += 32) ok = ok && wait_count(p.bar + kSlotWord + j, ready, p.status);
+    if (s0 && lane == 0) ok = ok && wait_count(p.bar + kSharedWord, ready, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0 && !ok) m.scalars[4] = 1;
   }
   bar_sync_named(1, kCons * 32);
   dead = m.scalars[4] != 0;  // one answer for the whole CTA from here on
+  bool broken = m.scalars[5] != 0;
   // Q8(h) rows by sorted position: the last ring stage (idle once every
   // gate/up item is consumed; the down items skip it) or the region of Q8(x)
   const uint32_t hq = smem_addr(smem + (p.hqr ? (size_t)(nstage - 1) * p.stage_bytes : (size_t)p.off_hq));
@@ -809,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   for (int it = nslot; it < nslot + ndi; ++it) {
     int st, use;
     ring_slot(it, nslot, nstage, p.hqr, st, use);
-    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), use & 1, p.status));
+    if (!broken && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), use & 1, p.status))) broken = dead = true;
     if (!dead) {
       const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
       for (int j = j0 + grp; j < j1; j += 2) {
@@ -993,23 +1011,14 @@ extern "C" int moe_decode_max_tokens(int H, int E, int k, int I) { return max_to
 
 extern "C" int moe_decode_max_tokens_shared(int H, int E, int k, int I) { return max_tokens(H, E, k, I, true); }
 
-namespace {
-
-// The shared expert's arguments of moe_decode_forward_shared.
-struct SharedArgs {
-  const uint8_t *wg, *sg, *wu, *su, *wd, *sd;
-  float *h;
-  int64_t ld_h;
-  float *y;
-  int64_t ld_y;
-};
+namespace moe {
 
 moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
                           moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg, const uint8_t *wu,
                           const uint8_t *su, const uint8_t *wd, const uint8_t *sd, int T, int H, int E, int k, int I,
                           float *out, int64_t ld_out, float *logits, int32_t *ids, float *weights, float *h,
                           int64_t ld_h, float *y, int64_t ld_y, void *workspace, size_t ws_bytes,
-                          const SharedArgs *sh, void *stream) {
+                          const SharedArgs *sh, bool clear_ws, void *stream) {
   if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0) return fail(MOE_ERR_INVALID_ARG, "%s: T=%d H=%d E=%d k=%d I=%d", name, T, H, E, k, I);
   if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad x dtype", name);
   if (w_dtype != MOE_F32 && w_dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "%s: bad router dtype", name);
@@ -1077,12 +1086,11 @@ moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, in
           (!sh || ((uintptr_t)sh->sg % 16 == 0 && (uintptr_t)sh->su % 16 == 0));
   p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0 && (!sh || (uintptr_t)sh->sd % 16 == 0);
 
-  static bool configured[36][64] = {};
-  const int ki = (SGp == 1 ? 0 : SGp == 2 ? 1 : 2) * 3 + (SDp == 1 ? 0 : SDp == 2 ? 1 : 2) + (full ? 9 : 0) + (sh ? 18 : 0);
-  if (dev < 64 && !configured[ki][dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), optin - 1024, name);
+  if (ast != MOE_OK) return ast;
+  if (clear_ws) {  // every check has passed: only now is anything enqueued
+    err = cudaMemsetAsync(workspace, 0, moe_decode_workspace_bytes(), static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return cuda_fail(err, name);
-    configured[ki][dev] = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(G);
@@ -1098,7 +1106,7 @@ moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, in
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
 }
 
-}  // namespace
+}  // namespace moe
 
 extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
                                          moe_dtype w_dtype, const float *bias, const uint8_t *wg, const uint8_t *sg,
@@ -1108,7 +1116,7 @@ extern "C" moe_status moe_decode_forward(const void *x, moe_dtype x_dtype, int64
                                          float *y, int64_t ld_y, void *workspace, size_t ws_bytes, void *stream) {
   return decode_forward("moe_decode_forward", x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd, T, H,
                         E, k, I, out, ld_out, logits, ids, weights, h, ld_h, y, ld_y, workspace, ws_bytes, nullptr,
-                        stream);
+                        false, stream);
 }
 
 extern "C" moe_status moe_decode_forward_shared(const void *x, moe_dtype x_dtype, int64_t ld_x, const void *w_router,
@@ -1126,5 +1134,5 @@ extern "C" moe_status moe_decode_forward_shared(const void *x, moe_dtype x_dtype
                       shared_h, ld_shared_h, shared_y, ld_shared_y};
   return decode_forward("moe_decode_forward_shared", x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd,
                         T, H, E, k, I, out, ld_out, logits, ids, weights, h, ld_h, y, ld_y, workspace, ws_bytes, &sh,
-                        stream);
+                        false, stream);
 }

@@ -15,10 +15,11 @@
 // library holds kScratchBytes of it until the process exits.  Host code must
 // never use the variable's name as a pointer: on the host it is a stand-in
 // symbol, not a device address.  Its device address is looked up with
-// cudaGetSymbolAddress once per device, on the first call made with that
-// device current.
-#include <mutex>
-
+// cudaGetSymbolAddress on every call, with the caller's device current (a
+// host-side query, no stream work; the first call on a device also loads the
+// module there, which is why that first call should come before any stream
+// capture).  Looking it up each time keeps a call correct after
+// cudaDeviceReset or in a new primary context.
 #include "common.cuh"
 
 namespace moe {
@@ -39,24 +40,12 @@ static_assert(kOffH % 256 == 0, "h rows must stay 16-byte aligned");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-unsigned char *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of this device's copy of the scratch array (set-up on first use).
+// Device address of the current device's copy of the scratch array.
 moe_status scratch_for_current_device(unsigned char **out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_decode_forward_noalloc: cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "moe_decode_forward_noalloc: device %d", dev);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (err != cudaSuccess || !ptr) return cuda_fail(err, "moe_decode_forward_noalloc: cudaGetSymbolAddress");
-    g_scratch_ptr[dev] = static_cast<unsigned char *>(ptr);
-  }
-  *out = g_scratch_ptr[dev];
+  void *ptr = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (err != cudaSuccess || !ptr) return cuda_fail(err, "moe_decode_forward_noalloc: cudaGetSymbolAddress");
+  *out = static_cast<unsigned char *>(ptr);
   return MOE_OK;
 }
 
@@ -84,11 +73,11 @@ extern "C" moe_status moe_decode_forward_noalloc(const void *x, moe_dtype x_dtyp
   if (st != MOE_OK) return st;
   // The barrier counter and its hold word must start at zero (the kernel
   // clears the readiness words itself); the other regions are written before
-  // they are read within one launch.
-  cudaError_t err = cudaMemsetAsync(s + kOffBar, 0, kBarBytes, static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return cuda_fail(err, "moe_decode_forward_noalloc: clearing the barrier words");
-  return moe_decode_forward(x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd, T, H, E, k, I, out,
-                            ld_out, reinterpret_cast<float *>(s + kOffLogits), reinterpret_cast<int32_t *>(s + kOffIds),
-                            reinterpret_cast<float *>(s + kOffW), reinterpret_cast<float *>(s + kOffH), I, nullptr, 0,
-                            s + kOffBar, kBarBytes, stream);
+  // they are read within one launch.  decode_forward clears the barrier
+  // words on the stream only after every argument check has passed, so a
+  // rejected call enqueues nothing.
+  return decode_forward(name, x, x_dtype, ld_x, w_router, w_dtype, bias, wg, sg, wu, su, wd, sd, T, H, E, k, I, out,
+                        ld_out, reinterpret_cast<float *>(s + kOffLogits), reinterpret_cast<int32_t *>(s + kOffIds),
+                        reinterpret_cast<float *>(s + kOffW), reinterpret_cast<float *>(s + kOffH), I, nullptr, 0,
+                        s + kOffBar, kBarBytes, nullptr, true, stream);
 }

@@ -349,26 +349,6 @@ MOE_DEVFN void load_weights(uint32_t wbase, uint32_t wstride, uint32_t sbase, ui
   }
 }
 
-// The same blocks kept packed (4 words per block), for callers that convert
-// per row (fewer live registers; the integer dots are the same).
-template <int NM, int S>
-MOE_DEVFN void load_weights_packed(uint32_t wbase, uint32_t wstride, uint32_t sbase, uint32_t sstride, int r, int K,
-                                   uint4 (&wr)[NM][S], float (&ws)[NM][S]) {
-  const int lane = threadIdx.x & 31;
-  const int nb = K / 32;
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-      const int b = lane + 32 * s;
-      if (b < nb) {
-        wr[m][s] = lds128(wbase + m * wstride + (uint32_t)r * (K / 2) + 16u * b);
-        ws[m][s] = e8m0_half(lds_u8(sbase + m * sstride + (uint32_t)r * nb + b));
-      }
-    }
-  }
-}
-
 // Block term of one activation block against the converted weights:
 // acc[m] = fma(float(I_b), sx * ws, acc[m]), I_b = dot(x, 12 + 2v) - 12*sum(x).
 template <int NM, int S>
@@ -403,39 +383,6 @@ MOE_DEVFN void row_dot_smem(uint32_t row, int K, const uint32_t (&wq)[NM][S][8],
       const float sx = lds_f32(row + (uint32_t)K + 4u * b);
       const int xsum = lds_s32(row + (uint32_t)K + 4u * (nb + b));
       block_terms<NM, S>(s, lo, hi, sx, xsum, wq, ws, acc);
-    }
-  }
-}
-
-// row_dot_smem with packed weights, converted block by block.
-template <int NM, int S>
-MOE_DEVFN void row_dot_smem_packed(uint32_t row, int K, const uint4 (&wr)[NM][S], const float (&ws)[NM][S],
-                                   float (&acc)[NM]) {
-  const int lane = threadIdx.x & 31;
-  const int nb = K / 32;
-#pragma unroll
-  for (int m = 0; m < NM; ++m) acc[m] = 0.0f;
-#pragma unroll
-  for (int s = 0; s < S; ++s) {
-    const int b = lane + 32 * s;
-    if (b < nb) {
-      const uint4 lo = lds128(row + 16u * b), hi = lds128(row + 16u * (nb + b));
-      const float sx = lds_f32(row + (uint32_t)K + 4u * b);
-      const int xsum = lds_s32(row + (uint32_t)K + 4u * (nb + b));
-      const uint32_t xw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        uint32_t q[8];
-        e2m1x8_to_off12(wr[m][s].x, q[0], q[1]);
-        e2m1x8_to_off12(wr[m][s].y, q[2], q[3]);
-        e2m1x8_to_off12(wr[m][s].z, q[4], q[5]);
-        e2m1x8_to_off12(wr[m][s].w, q[6], q[7]);
-        int d = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) d = __dp4a((int)xw[j], (int)q[j], d);
-        const int I = d - 12 * xsum;
-        acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, ws[m][s]), acc[m]);
-      }
     }
   }
 }

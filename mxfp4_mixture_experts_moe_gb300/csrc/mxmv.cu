@@ -275,14 +275,9 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + (p.act_smem ? act_bytes : 0);
   const dim3 block((ncons + 1) * 32);
 
-  static bool configured[3][3][64] = {};
-  const int si = S == 1 ? 0 : (S == 2 ? 1 : 2);
   auto kern = S == 1 ? mx_expert_kernel<MODE, 1> : (S == 2 ? mx_expert_kernel<MODE, 2> : mx_expert_kernel<MODE, 4>);
-  if (dev < 64 && !configured[MODE][si][dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-    if (err != cudaSuccess) return cuda_fail(err, name);
-    configured[MODE][si][dev] = true;
-  }
+  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)budget, name);
+  if (ast != MOE_OK) return ast;
   kern<<<G, block, smem, stream>>>(p);
   err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);

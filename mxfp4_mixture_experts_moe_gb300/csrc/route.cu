@@ -115,18 +115,10 @@ cudaError_t launch_route_logits(const void *x, int64_t ld_x, const void *wr, int
   constexpr uint32_t smem = 2u * (kRouteWarps * EW * kRouteSlab * 8 * (WBF ? 2 : 4) +
                                   kRouteTokens * kRouteSlab * 8 * (XBF ? 2 : 4));
   static_assert(smem <= 227 * 1024, "slabs fit shared memory");
-  if (smem > 48 * 1024) {
-    static bool done[64] = {};  // per device; setting it twice (racing threads) is harmless
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(route_logits_kernel<EW, XBF, WBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) done[dev] = true;
-    }
-  }
+  if (smem > 48 * 1024 &&
+      ensure_smem_attr(reinterpret_cast<const void *>(route_logits_kernel<EW, XBF, WBF>), (int)smem,
+                       "moe_route_topk") != MOE_OK)
+    return cudaErrorInvalidValue;
   dim3 grid((E + kRouteWarps * EW - 1) / (kRouteWarps * EW), (T + kRouteTokens - 1) / kRouteTokens);
   route_logits_kernel<EW, XBF, WBF><<<grid, kRouteWarps * 32, smem, s>>>(x, ld_x, wr, T, H, E, logits);
   return cudaGetLastError();

@@ -124,14 +124,9 @@ extern "C" moe_status moe_sort_tokens(const int32_t *ids, int T, int k, int E, i
   if (A > 0 && (!ids || !inv)) return fail(MOE_ERR_INVALID_ARG, "moe_sort_tokens: null pointer");
   if (cap < need || (need > 0 && !sorted)) return fail(MOE_ERR_INVALID_ARG, "moe_sort_tokens: cap=%lld < %lld", (long long)cap, (long long)need);
   const size_t smem = sizeof(int) * (size_t)E * 35;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 35 * 1024 * 4);
-    if (err != cudaSuccess) return cuda_fail(err, "moe_sort_tokens: smem attribute");
-    configured[dev] = 1;
-  }
+  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(sort_kernel), 35 * 1024 * 4,
+                                         "moe_sort_tokens: smem attribute");
+  if (ast != MOE_OK) return ast;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   sort_kernel<<<1, kSortThreads, smem, s>>>(ids, (int)A, E, tile_rows, offsets, sorted, inv, device_status_word());
   cudaError_t err = cudaGetLastError();

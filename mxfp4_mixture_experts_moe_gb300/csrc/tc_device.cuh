@@ -1,38 +1,22 @@
 // 5th-generation tensor-core (tcgen05) building blocks: tensor-memory
-// allocation, shared-memory operand descriptors, the MMA issue, its commit to
-// an mbarrier, and the tensor-memory loads of the accumulator.
+// allocation, shared-memory operand descriptors, the MMA commit to an
+// mbarrier, tensor-memory stores, and the fences around them.
 //
-// Operand layout used throughout (PTX ISA, "tcgen05 matrix descriptors",
-// K-major, no swizzle): a tile of R rows x 64 f16 elements is stored as
-// 8 x 8 "core matrices" of 8 rows x 16 bytes, each 128 contiguous bytes.
-// The core matrices of one 8-row group follow each other along K (leading
-// byte offset 128), and the 8-row groups follow each other (stride byte
-// offset 1024).  Element (r, k) of a tile is at byte
-//     (r / 8) * 1024 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
+// Operand layout of a descriptor without swizzle (PTX ISA, "tcgen05 matrix
+// descriptors", K-major): "core matrices" of 8 rows x 16 bytes, each 128
+// contiguous bytes; the leading byte offset steps to the next core matrix
+// along K, the stride byte offset to the next 8-row group.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-constexpr uint32_t kCoreLbo = 128;   // next core matrix along K
-constexpr uint32_t kCoreSbo = 1024;  // next 8-row group (64 K elements per row)
-
-MOE_DEVFN uint32_t tile_offset(int r, int k) {
-  return (uint32_t)(r >> 3) * kCoreSbo + (uint32_t)(k >> 3) * kCoreLbo + (uint32_t)(r & 7) * 16u + (uint32_t)(k & 7) * 2u;
-}
-
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (all >> 4), descriptor version 1, no swizzle.
 MOE_DEVFN uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor of kind::f16 with f16 A and B, f32 accumulator,
-// both operands K-major, shape M x N.
-MOE_DEVFN uint32_t idesc_f16(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Allocation of ncols tensor-memory columns by one whole warp; the base
@@ -45,30 +29,10 @@ MOE_DEVFN void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-MOE_DEVFN void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-
 // The mbarrier at bar gets one arrival when every MMA issued so far by this
 // thread has completed (its shared-memory operands may then be reused).
 MOE_DEVFN void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T with A in tensor memory: row m of A in
-// lane m, K along the columns, two f16 elements per 32-bit column (even k in
-// the low half).  Issued by one thread.
-MOE_DEVFN void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
 }
 
 MOE_DEVFN void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -76,39 +40,6 @@ MOE_DEVFN void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync
 
 // Generic-proxy shared-memory writes made visible to the tensor core.
 MOE_DEVFN void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// 32 consecutive columns of this warp's 32 lanes (warp w reads lanes
-// 32*(w%4) .. +31; the lane bits of taddr must say so).
-MOE_DEVFN void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-
-// 16 consecutive columns of this warp's 32 lanes.
-MOE_DEVFN void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // Store of 32 registers into 32 consecutive columns of this warp's 32 lanes
 // (asynchronous: tmem_st_wait() before the values are handed on).

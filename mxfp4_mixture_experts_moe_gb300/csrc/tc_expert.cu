@@ -713,12 +713,8 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
   const size_t smem = (size_t)p.off_misc + tc_shared_bytes(E) + 1024u;  // + alignment of the base
   if (smem > (size_t)optin) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs %zu bytes of shared memory", name, smem);
   auto kern = mode == kSwiglu ? tc_expert_kernel<kSwiglu> : mode == kRaw ? tc_expert_kernel<kRaw> : tc_expert_kernel<kDownMode>;
-  static bool configured[3][64] = {};
-  if (dev < 64 && !configured[mode][dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (err != cudaSuccess) return cuda_fail(err, name);
-    configured[mode][dev] = true;
-  }
+  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), optin, name);
+  if (ast != MOE_OK) return ast;
   kern<<<sm_count(), kThreads, smem, stream>>>(p, maps);
   err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);

@@ -117,13 +117,16 @@ def test_fused_graph_replay(moe, dsv4):
         assert bits_equal(host(ws.out), ref), i
 
 
-def test_fused_barrier_timeout_is_reported(moe, dsv4):
+@pytest.mark.parametrize("T", [1, 4])
+def test_fused_barrier_timeout_is_reported(moe, dsv4, T):
     """A grid barrier that can never complete (the workspace's hold word
     raises every barrier's target above the number of CTAs) must give up
     within its time bound, raise MOE_DEV_WAIT_TIMEOUT and return; with the
-    hold cleared the next call works again."""
-    x = dev(synth.activations(synth.DSV4, 1, token0=10))
-    ws = moe.Workspace(1, dsv4, "cuda")
+    hold cleared the next call works again.  T = 4 is a shape whose Q8(h)
+    rows take the ring's last stage in the down phase, so the producer's
+    exit drain must find that stage's last copy among the gate/up items."""
+    x = dev(synth.activations(synth.DSV4, T, token0=10))
+    ws = moe.Workspace(T, dsv4, "cuda")
     layer = moe.MoeLayer(dsv4, fused=True)
     layer.forward(x, ws)
     assert moe.moe_device_status() == 0
@@ -132,6 +135,31 @@ def test_fused_barrier_timeout_is_reported(moe, dsv4):
     layer.forward(x, ws)
     assert moe.moe_device_status() & moe.MOE_DEV_WAIT_TIMEOUT
     ws.decode_ws[1] = 0
+    ws.out.zero_()
+    layer.forward(x, ws)
+    assert moe.moe_device_status() == 0
+    assert bits_equal(host(ws.out), ref)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_fused_readiness_timeout_is_reported(moe, dsv4, T):
+    """The wait for every CTA's h slices (the per-expert readiness words) runs
+    out when the workspace's readiness hold raises its target above the
+    number of CTAs.  The kernel must raise MOE_DEV_WAIT_TIMEOUT and return;
+    its consumer warps still wait (bounded) for each ring copy before they
+    release its stage, so the producer never re-arms a stage with a copy in
+    flight and leaves none behind.  With the hold cleared the next call gives
+    the bits of the call before."""
+    x = dev(synth.activations(synth.DSV4, T, token0=11))
+    ws = moe.Workspace(T, dsv4, "cuda")
+    layer = moe.MoeLayer(dsv4, fused=True)
+    layer.forward(x, ws)
+    assert moe.moe_device_status() == 0
+    ref = host(ws.out).copy()
+    ws.decode_ws[2] = 1
+    layer.forward(x, ws)
+    assert moe.moe_device_status() & moe.MOE_DEV_WAIT_TIMEOUT
+    ws.decode_ws[2] = 0
     ws.out.zero_()
     layer.forward(x, ws)
     assert moe.moe_device_status() == 0

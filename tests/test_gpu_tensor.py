@@ -2,9 +2,9 @@
 batches of more than 16 rows, against the oracle.
 
 The tensor path keeps the layer's exact block dots: E2M1 weights with their
-E8M0 byte as the MMA block scale, the Q8 codes as four base-4 digit planes,
-one fp32 accumulator per block (exact), then acc = fma(D, xs, acc) block by
-block.  With unit scales every block term is an integer and every output is
+E8M0 byte as the MMA block scale, the Q8 codes as three base-8 digit
+planes, one fp32 accumulator per block (exact), then acc = fma(D, xs, acc)
+block by block.  With unit scales every block term is an integer and every output is
 exact, so those cases are compared bit for bit with the oracle; with the
 layer's scales the order of the fp32 accumulation differs from the oracle's,
 so the bar is the layer's tolerance, max|err| <= 1e-3 * RMS.  Cases span
