@@ -41,16 +41,27 @@
  *  - Values the host cannot see (expert ids, sort offsets) are bounds-checked
  *    on the device; an out-of-range value is skipped and raises a bit in the
  *    device status word, read by moe_device_status().
- *  - Deterministic: no floating-point atomics.  Every row's result is computed
- *    by the same arithmetic whatever the number of rows T in the call, so a
- *    T-row call gives, row by row, the bits of T one-row calls.
+ *  - Deterministic: no floating-point atomics; the same call on the same
+ *    inputs gives the same bits.
+ *  - Exact rows ("The exact-rows contract" of the Strix Halo record): for
+ *    T <= 16 rows every row's result is computed by the arithmetic of the
+ *    one-row call, so a T-row call gives, row by row, the bits of T one-row
+ *    calls (stage calls and the single-launch decode path alike).  Routing,
+ *    the sorter, Q8 and the combine keep that for every T.  From 17 rows on,
+ *    the expert projections of experts with many rows run on the tensor
+ *    cores, which form the same exact block terms but add them in increasing
+ *    block order: those rows agree with the one-row call within fp32
+ *    rounding (the layer's tolerance), not bit for bit.
  *  - Requires an sm_103a device (GB300); MOE_ERR_UNSUPPORTED otherwise.
  *
  * Weight layout (one layer; E experts; all contiguous, 16-byte aligned):
  *  - wg, wu: uint8 [E][I][H/2]; byte c of a row holds element 2c in its low
  *    nibble and 2c+1 in its high nibble; a nibble is an E2M1 code (OCP MX).
  *  - sg, su: uint8 [E][I][H/32]; one E8M0 byte (2^(u-127); 255 = NaN) per 32
- *    consecutive elements of a row.
+ *    consecutive elements of a row.  Every byte 0..255 is accepted; a block
+ *    term is I_b * (xs_b * 2^(u-128)) in fp32, so results match the exact
+ *    value within fp32 rounding wherever that scale product and the sums
+ *    are finite fp32 numbers (byte 255 makes the outputs it reaches NaN).
  *  - wd: uint8 [E][H][I/2], sd: uint8 [E][H][I/32], same conventions.
  */
 #ifndef MOE_MXFP4_H
@@ -110,7 +121,9 @@ MOE_API moe_status moe_device_status(void *stream, uint32_t *flags);
  *           increasing order, one fused multiply-add per element), then the 32
  *           partials are added pairwise p[l] += p[l+s], s = 16, 8, 4, 2, 1.
  *  ids      [T][k] int32 output: the k experts of largest score = logit + bias,
- *           ties to the lower id, in descending score order.
+ *           ties to the lower id, in descending score order.  A NaN score
+ *           is never taken; a slot for which only NaN scores are left gets
+ *           the id 0x7fffffff (no expert) and weight 0.
  *  weights  [T][k] fp32 output: sigmoid(score) renormalised over the k slots.
  * Requires H % 8 == 0, 1 <= k <= min(E, 8), E <= 1024; x and w_router
  * 16-byte aligned, ld_x * element size a multiple of 16 bytes. */
@@ -162,8 +175,9 @@ MOE_API moe_status act_quant_q8(const void *x, moe_dtype x_dtype, int rows, int 
  *   I_b  = exact integer sum over the 32 elements of block b of
  *          xq[t,.] * (2 * E2M1 value)  (twice the E2M1 value is an integer),
  *   h[a, i] = silu(G[i]) * U[i],   silu(g) = g / (1 + exp(-g)).
- * Scaled block terms are accumulated in fp32 in a fixed order independent of
- * the number of rows.  One pass over an expert's weights serves all its rows.
+ * Scaled block terms are accumulated in fp32 in a fixed order; for T <= 16
+ * that order does not depend on the number of rows (see "Exact rows" above).
+ * One pass over an expert's weights serves all its rows.
  *  xq [T][ld_xq] int8, xs [T][ld_xs] fp32  (Q8 of the activations).
  *  offsets [E+1], sorted [cap] from moe_sort_tokens.
  *  h [T*k][ld_h] fp32 output; rows of assignments not in `sorted` untouched.
@@ -204,7 +218,9 @@ MOE_API moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *
 
 /* Routing-weighted combine in slot order (the gfx90a report, §8.2 "FP32 top-k
  * partial and fixed reduction"): out[t,n] = fma(w[t,k-1], y[t*k+k-1,n], ...
- * fma(w[t,1], y[t*k+1,n], w[t,0]*y[t*k,n])), fp32.
+ * fma(w[t,1], y[t*k+1,n], w[t,0]*y[t*k,n])), fp32.  A slot of weight exactly
+ * 0 adds nothing and its y row is not read (top-k gives that weight to a slot
+ * with no expert, whose y row no projection writes).
  *  y [T*k][ld_y], w [T][k] fp32; out [T][ld_out] fp32 output. */
 MOE_API moe_status moe_combine(const float *y, int64_t ld_y, const float *w, int T, int k, int H,
                        float *out, int64_t ld_out, void *stream);

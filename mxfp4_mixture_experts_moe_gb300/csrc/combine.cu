@@ -3,7 +3,10 @@
 // "DeepSeek-V4-Flash on AMD gfx90a", §8.2: the down consumer "retains the
 // existing FP32 top-k partial and fixed reduction"; Table 4 ("BF16 down
 // partial ... retain FP32 partials").  out[t,n] = fma chain over j = 0..k-1,
-// fp32, the same for every token whatever T is.
+// fp32, the same for every token whatever T is.  A slot whose weight is
+// exactly 0 adds nothing and its y row is not read: top-k gives that weight
+// to a slot with no expert (only NaN scores were left for it), whose y row
+// no projection writes.
 #include "common.cuh"
 
 namespace moe {
@@ -16,8 +19,9 @@ combine_kernel(const float *y, int64_t ld_y, const float *w, int T, int k, int H
   const int t = (int)(gid / H), n = (int)(gid % H);
   const float *wt = w + (int64_t)t * k;
   const float *yt = y + (int64_t)t * k * ld_y + n;
-  float acc = __fmul_rn(wt[0], yt[0]);
-  for (int j = 1; j < k; ++j) acc = __fmaf_rn(wt[j], yt[(int64_t)j * ld_y], acc);
+  float acc = wt[0] != 0.0f ? __fmul_rn(wt[0], yt[0]) : 0.0f;
+  for (int j = 1; j < k; ++j)
+    if (wt[j] != 0.0f) acc = __fmaf_rn(wt[j], yt[(int64_t)j * ld_y], acc);
   out[(int64_t)t * ld_out + n] = acc;
 }
 

@@ -869,8 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   for (int idx = tid; idx < T * Rd; idx += kCons * 32) {
     const int t = idx / Rd, r = idx - t * Rd;
     const float *wt = m.w + t * k;
-    float acc = __fmul_rn(wt[0], yslice[(t * k) * p.Rd + r]);
-    for (int j = 1; j < k; ++j) acc = __fmaf_rn(wt[j], yslice[(t * k + j) * p.Rd + r], acc);
+    // (as the stand-alone combine: a slot of weight exactly 0 adds nothing)
+    float acc = wt[0] != 0.0f ? __fmul_rn(wt[0], yslice[(t * k) * p.Rd + r]) : 0.0f;
+    for (int j = 1; j < k; ++j)
+      if (wt[j] != 0.0f) acc = __fmaf_rn(wt[j], yslice[(t * k + j) * p.Rd + r], acc);
     if (s0) acc = __fadd_rn(acc, yslice[(A + t) * p.Rd + r]);  // the shared expert's join
     p.out[(int64_t)t * p.ld_out + n0d + r] = acc;
   }

@@ -11,23 +11,29 @@
 //
 // Every block dot is exact, as in the CUDA-core kernels.  The tensor core
 // takes the weights as they are stored: E2M1 nibbles (kind::mxf4, K = 64 per
-// MMA = two MX blocks) with the weight's E8M0 byte as the block scale of A.
+// MMA = two MX blocks) with the weight's E8M0 byte u as the block scale of A,
+// clamped to uc = min(max(u, 64), 192) so that every partial sum of the MMA
+// is an exact normal fp32 number; the drain multiplies the activation scale
+// by the remainder 2^(u - uc) (NaN for byte 255) when a byte lies outside
+// that range (no real checkpoint has one; the multiply is skipped when all 32
+// rows of a warp are inside it).
 // The Q8 codes q of the activations are not an MMA type, so each is written
 // as three signed base-8 digits q = d0 + 8 d1 + 64 d2, d0, d1 in {-4..3} and
 // d2 in {-2..2} (every q in [-128, 127] has this form), each an exact E2M1
 // value; plane i is an MMA operand with block scale 8^i.  The three plane
 // MMAs sum into one fp32 accumulator:  D = 2^(u-127) * sum_k v_k q_k =
 // I_b 2^(u-128) with I_b the integer block dot of twice the E2M1 values;
-// every partial sum is a multiple of 2^(u-128) below 2^(u-110), exact in
-// fp32.  Every MMA accumulates (a block-scaled MMA that overwrites its
+// every partial sum is a multiple of 2^(uc-128) below 2^(uc-110), exact in
+// fp32 (uc = u inside the clamp range).  Every MMA accumulates (a block-scaled MMA that overwrites its
 // accumulator costs several times one that adds to it); the drain sets each
 // accumulator buffer back to zero after reading it.  To keep the
 // two blocks of a K-step apart, the B operand has two rows per activation
 // row: rows [0, 32) carry the even block of each K-step (zeros in the odd
 // one), rows [32, 64) the odd block.  The epilogue of each K-step ("drain")
-// then forms  acc = fma(D, xs_b, acc)  per (weight row, activation row,
-// block), which equals the CUDA-core term fma(I_b, xs_b * 2^(u-128), acc):
-// the same exact product, one rounding.  Blocks are accumulated in
+// then forms  acc = fma(D, xs_b * 2^(u-uc), acc)  per (weight row,
+// activation row, block), which equals the CUDA-core term
+// fma(I_b, xs_b * 2^(u-128), acc): the same exact product, one rounding
+// (both scale products are exact whenever they are normal numbers).  Blocks are accumulated in
 // increasing order; the CUDA-core kernels add per-lane partial sums in a
 // butterfly instead, so the two paths agree within fp32 rounding, not bit
 // for bit.
@@ -78,6 +84,18 @@ constexpr int kMaxDBuf = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaBase = 16;   // columns [0, 12): B scales, plane i at 4 i
 constexpr uint32_t kDBase = 128;    // first accumulator column
+constexpr uint32_t kUcLo = 0x40404040u;  // E8M0 bytes given to the MMA: clamped to [64, 192]
+constexpr uint32_t kUcHi = 0xC0C0C0C0u;
+
+// Four E8M0 bytes clamped to the MMA's range.
+MOE_DEVFN uint32_t clamp_e8m0x4(uint32_t w) { return __vmaxu4(__vminu4(w, kUcHi), kUcLo); }
+// Non-zero when one of four E8M0 bytes lies outside the MMA's range.
+MOE_DEVFN uint32_t outside_e8m0x4(uint32_t w) { return __vcmpltu4(w, kUcLo) | __vcmpgtu4(w, kUcHi); }
+// 2^(u - uc) for an E8M0 byte u and its clamped value uc (exact; NaN for 255).
+MOE_DEVFN float e8m0_remainder(uint32_t u) {
+  const uint32_t uc = u < 64u ? 64u : (u > 192u ? 192u : u);
+  return u == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float((127u + u - uc) << 23);
+}
 
 enum Mode { kSwiglu = 0, kRaw = 1, kDownMode = 2 };
 
@@ -114,6 +132,7 @@ struct TcShared {
   int colrow[2][kNT]; // activation row of each column (-1: none)
   int colasg[2][kNT]; // output row (assignment) of each column (-1: none)
   uint32_t lut[2][256];  // Q8 code -> its four digit codes, low / high nibble of byte i = plane i
+  int ext[kMaxStages][4];  // per stage slot and lane quadrant: an E8M0 byte outside the MMA's clamp range
   int prefix[1];         // [E + 1] tiles before expert e
 };
 
@@ -223,6 +242,31 @@ MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   tl.col0 = b + ntile * kNT;
   tl.ncols = min(kNT, n_e - ntile * kNT);
   return tl;
+}
+
+// The drain's K-step for a warp whose rows hold an E8M0 byte outside the
+// MMA's clamp range: acc = fma(D, xs * 2^(u - uc), acc) per matrix, block and
+// column, D = I_b 2^(uc-128).  A separate, never-inlined function, so that
+// the rare case costs the common one no registers.  sb: offset of the
+// K-step's two bytes in this row's E8M0 bytes of each matrix.
+template <int NM>
+__device__ __noinline__ void drain_remainders(float (&acc)[NM][16], uint32_t dcol, const float (&x0)[16],
+                                              const float (&x1)[16], const uint8_t *s0, const uint8_t *s1,
+                                              int64_t sb) {
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const uint32_t w2 = __ldg(reinterpret_cast<const unsigned short *>((m == 0 ? s0 : s1) + sb));
+    const float f0 = e8m0_remainder(w2 & 0xFFu), f1 = e8m0_remainder((w2 >> 8) & 0xFFu);
+    uint32_t de[16], dd[16];
+    tmem_ld16_nowait(dcol + (uint32_t)m * kN, de);
+    tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      acc[m][c] = __fmaf_rn(__uint_as_float(de[c]), __fmul_rn(x0[c], f0), acc[m][c]);
+      acc[m][c] = __fmaf_rn(__uint_as_float(dd[c]), __fmul_rn(x1[c], f1), acc[m][c]);
+    }
+  }
 }
 
 template <int MODE>
@@ -341,6 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         // on before this warp releases the slot)
         ok = warp_wait(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
         if (!ok) break;
+        // the MMA saw the E8M0 bytes of this quadrant's rows clamped; if one
+        // lay outside the clamp range, the remainders are applied (the two
+        // bytes of each K-step are read again for that)
+        const bool ext = S.ext[slot][q] != 0;
         for (int s = 0; s < kSteps; ++s) {
           const int j = g * kSteps + s, db = j % ND;
           ok = warp_wait(smem_addr(&S.d_full[db]), (j / ND) & 1, p.status);
@@ -348,13 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
           tc_fence_after();
           if (active) {
             const uint32_t dcol = tmem + lanes + kDBase + (uint32_t)db * NM * kN + 16u * h;
-            uint32_t de[NM][16], dd[NM][16];
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              tmem_ld16_nowait(dcol + (uint32_t)m * kN, de[m]);
-              tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd[m]);
-            }
-            tmem_ld_wait();
             // scales of blocks 8 st + 2 s and + 1 of columns 16 h .. 16 h + 15
             float x0[16], x1[16];
 #pragma unroll
@@ -366,13 +407,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
               x1[4 * v] = __uint_as_float(b.x); x1[4 * v + 1] = __uint_as_float(b.y);
               x1[4 * v + 2] = __uint_as_float(b.z); x1[4 * v + 3] = __uint_as_float(b.w);
             }
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            if (!ext) {
+              uint32_t de[NM][16], dd[NM][16];
 #pragma unroll
               for (int m = 0; m < NM; ++m) {
-                acc[m][c] = __fmaf_rn(__uint_as_float(de[m][c]), x0[c], acc[m][c]);
-                acc[m][c] = __fmaf_rn(__uint_as_float(dd[m][c]), x1[c], acc[m][c]);
+                tmem_ld16_nowait(dcol + (uint32_t)m * kN, de[m]);
+                tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd[m]);
               }
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+#pragma unroll
+                for (int m = 0; m < NM; ++m) {
+                  acc[m][c] = __fmaf_rn(__uint_as_float(de[m][c]), x0[c], acc[m][c]);
+                  acc[m][c] = __fmaf_rn(__uint_as_float(dd[m][c]), x1[c], acc[m][c]);
+                }
+              }
+            } else {
+              drain_remainders<NM>(acc, dcol, x0, x1, p.s0, p.s1, (S.wrow[tb] + r) * (int64_t)(K / 32) + st * 8 + 2 * s);
             }
           }
           {
@@ -502,13 +554,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
             sts128(bst + (uint32_t)pl * kBPlane + off, make_uint4(pw[pl][0], pw[pl][1], pw[pl][2], pw[pl][3]));
           sts32(s_xs + (uint32_t)slot * kXsStage + (uint32_t)(jb * kNT + c) * 4u, __float_as_uint(xsv[u]));
         }
+        // does one of this quadrant's rows hold an E8M0 byte outside the
+        // MMA's clamp range in this stage?
+        {
+          uint32_t outside = 0;
+#pragma unroll
+          for (int m = 0; m < NM; ++m) outside |= outside_e8m0x4(sfw[m].x) | outside_e8m0x4(sfw[m].y);
+          const int any = __any_sync(0xffffffffu, outside != 0);
+          if (lane == 0) S.ext[slot][q] = any;
+        }
         // A block scales of the stage: K-step s of matrix m at columns
         // kSfaBase + 4 (slot-local index) + quadrant, bytes 0 / 1 = its two blocks
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
 #pragma unroll
           for (int s = 0; s < kSteps; ++s) {
-            const uint32_t w2 = (s < 2 ? sfw[m].x : sfw[m].y) >> (16 * (s & 1));
+            const uint32_t w2 = clamp_e8m0x4(s < 2 ? sfw[m].x : sfw[m].y) >> (16 * (s & 1));
             const uint32_t col = kSfaBase + 4u * (uint32_t)((slot * kSteps + s) * NM + m) + (uint32_t)q;
             tmem_st1(tmem + lanes + col, w2 & 0xFFFFu);
           }

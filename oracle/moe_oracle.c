@@ -104,7 +104,14 @@ void moe_oracle_router_logits(const void *x, int x_bf16, int64_t ld_x,
  * presents selected positions in a fixed order".  READING: ties go to the
  * lower expert id; slots are ordered by descending score.  Weights are the
  * sigmoid of the selected scores renormalised to sum 1 (the tiny-layer
- * workload's "sigmoid scores, top-k renormalised"), computed in fp64. */
+ * workload's "sigmoid scores, top-k renormalised"), computed in fp64.
+ * READING (the pages say nothing of non-finite scores): a NaN score is never
+ * selected, since it names no ordering; a slot for which only NaN scores are
+ * left gets the id MOE_ORACLE_NO_EXPERT (0x7fffffff, an id no layer has) and
+ * the score -inf, so its sigmoid, and its weight, is 0.  An infinite score is
+ * an ordinary score (+inf first, -inf last, weight 0 for -inf). */
+#define MOE_ORACLE_NO_EXPERT 0x7fffffff
+
 void moe_oracle_topk(const float *logits, const float *bias, int T, int E, int k,
                      int32_t *ids, double *w)
 {
@@ -121,12 +128,19 @@ void moe_oracle_topk(const float *logits, const float *bias, int T, int E, int k
         for (int j = 0; j < k; ++j) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
-                if (taken[e]) continue;
+                if (taken[e] || isnan(score[e])) continue;
                 if (best < 0 || score[e] > score[best]) best = e; /* strict: lower id keeps ties */
             }
-            taken[best] = 1;
-            ids[(int64_t)t * k + j] = best;
-            sig[j] = 1.0 / (1.0 + exp(-(double)score[best]));
+            double s;
+            if (best < 0) {
+                ids[(int64_t)t * k + j] = MOE_ORACLE_NO_EXPERT;
+                s = -INFINITY;
+            } else {
+                taken[best] = 1;
+                ids[(int64_t)t * k + j] = best;
+                s = (double)score[best];
+            }
+            sig[j] = 1.0 / (1.0 + exp(-s));
             total += sig[j];
         }
         for (int j = 0; j < k; ++j) w[(int64_t)t * k + j] = sig[j] / total;
@@ -328,6 +342,15 @@ int moe_oracle_layer(const void *x, int x_bf16, int T, int H,
     int rc = 0;
     for (int64_t a = 0; a < A && rc == 0; ++a) {
         int t = (int)(a / k), e = ids[a];
+        if (e < 0 || e >= E) {
+            /* READING: a slot with no expert (moe_oracle_topk's NaN rule)
+             * contributes nothing: its h, Q8(h) and y rows are 0 (and its
+             * weight is 0). */
+            for (int i = 0; i < I; ++i) { h[a * I + i] = 0.0; hq[a * I + i] = 0; }
+            for (int b = 0; b < I / 32; ++b) hs[a * (I / 32) + b] = 0.0f;
+            for (int n = 0; n < H; ++n) y[a * H + n] = 0.0;
+            continue;
+        }
         if (!wg[e] || !sg[e] || !wu[e] || !su[e] || !wd[e] || !sd[e]) { rc = -1; break; }
         moe_oracle_expert_gateup(xq + (int64_t)t * H, xs + (int64_t)t * (H / 32),
                                  wg[e], sg[e], wu[e], su[e], H, I, G, U);

@@ -168,13 +168,45 @@ def test_fused_readiness_timeout_is_reported(moe, dsv4, T):
 
 def test_fused_nan_scores_are_flagged_not_followed(moe, dsv4):
     """NaN activations make every router score NaN, so top-k has no valid
-    expert.  The fused kernel must flag the ids and read no weights for them
-    (and not fault); the stage path's sorter does the same."""
+    expert: every slot gets the oracle's "no expert" id 0x7fffffff.  The
+    fused kernel must flag the ids and read no weights for them (and not
+    fault); the stage path's sorter does the same."""
     x = torch.full((1, 4096), float("nan"), dtype=torch.bfloat16, device="cuda")
     for fused in (True, False):
         ws = moe.Workspace(1, dsv4, "cuda")
         moe.MoeLayer(dsv4, fused=fused).forward(x, ws)
         assert moe.moe_device_status() & moe.MOE_DEV_BAD_EXPERT_ID
+        ref_ids, _ = oracle.topk(host(ws.logits), dsv4.k)
+        assert np.array_equal(host(ws.ids), ref_ids)
+        assert (ref_ids == 0x7FFFFFFF).all()
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_nan_router_rows_match_the_oracle(moe, T):
+    """Every router row but expert 3's is NaN, so each token's second slot has
+    no expert.  On the single launch and on the stage calls alike, the ids
+    (0x7fffffff for that slot), the weights (1 and 0) and the layer output
+    (the empty slot adds nothing) match the oracle, and the device status
+    flags the missing expert."""
+    spec = synth.TINY
+    wr = synth.router_weights(spec).copy()
+    wr[[e for e in range(spec.E) if e != 3]] = np.nan
+    lw = upload_layer(spec)
+    lw.wr = dev(wr)
+    xh = synth.activations(spec, T, token0=60)
+    r = oracle.layer(xh, wr, None, spec.k, {3: synth.expert(spec, 3)})
+    assert (r["ids"][:, 1] == 0x7FFFFFFF).all()
+    outs = []
+    for fused in (True, False):
+        ws = moe.Workspace(T, lw, "cuda")
+        ws.y.fill_(float("nan"))  # rows no projection writes must not be read
+        moe.MoeLayer(lw, fused=fused).forward(dev(xh), ws)
+        assert moe.moe_device_status() & moe.MOE_DEV_BAD_EXPERT_ID
+        assert np.array_equal(host(ws.ids), r["ids"])
+        assert np.allclose(host(ws.w), r["w"], rtol=1e-6, atol=0)
+        assert max_err_over_rms(host(ws.out), r["out"]) <= TOL
+        outs.append(host(ws.out))
+    assert bits_equal(outs[0], outs[1])
 
 
 def test_fused_single_expert_per_token(moe):

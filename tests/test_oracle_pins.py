@@ -255,6 +255,62 @@ def test_topk_ties_go_to_lower_id():
     assert list(ids[1]) == [0, 1, 2]
 
 
+NO_EXPERT = 0x7FFFFFFF
+
+
+def test_topk_nan_scores_are_never_taken():
+    """Brute force over rows with NaN scores sprinkled in (some rows keep
+    fewer than k real scores, one has none): the k best real scores by
+    (score desc, id asc), then slots with no expert (id 0x7fffffff, weight
+    0); weights are expit of the taken scores over their sum.  Infinite
+    scores are ordinary scores (+inf first, -inf last with weight 0)."""
+    from scipy.special import expit
+    T, E, k = 12, 16, 6
+    logits = synth.normal(3, 410, 0, T * E).astype(np.float32).reshape(T, E)
+    nan_mask = synth.uniform01(3, 411, 0, T * E).reshape(T, E) < 0.4
+    logits[nan_mask] = np.nan
+    logits[3, 12:] = np.nan          # row 3: only 12 real scores at most
+    logits[4, :] = np.nan            # row 4: none
+    logits[5, :E - 3] = np.nan       # row 5: 3 real scores < k
+    logits[6, 2], logits[6, 7] = np.inf, -np.inf
+    logits[7, :] = np.nan            # row 7: a real score and -inf, nothing else
+    logits[7, 1], logits[7, 5] = -np.inf, 0.3
+    ids, w = oracle.topk(logits, k)
+    for t in range(T):
+        real = [(-float(logits[t, e]), e) for e in range(E) if not np.isnan(logits[t, e])]
+        take = [e for _, e in sorted(real)[:k]]
+        ref_ids = take + [NO_EXPERT] * (k - len(take))
+        assert list(ids[t]) == ref_ids, t
+        sig = np.array([expit(float(logits[t, e])) for e in take] + [0.0] * (k - len(take)))
+        total = sig.sum()
+        if total > 0:
+            assert np.allclose(w[t], sig / total, rtol=1e-14, atol=0), t
+        else:
+            assert np.isnan(w[t]).all(), t
+    assert list(ids[4]) == [NO_EXPERT] * k
+    assert ids[6, 0] == 2
+    assert list(ids[7]) == [5, 1] + [NO_EXPERT] * (k - 2) and list(w[7]) == [1.0] + [0.0] * (k - 1)
+
+
+def test_layer_slot_without_expert_contributes_nothing():
+    """Every router row but expert 3's is NaN, so with k = 2 each token's
+    second slot has no expert: its id is 0x7fffffff, its weight 0, its h and
+    y rows 0, and the layer output equals the k = 1 layer's (expert 3 with
+    weight 1) exactly."""
+    spec = synth.TINY
+    x = synth.activations(spec, 3)
+    wr = synth.router_weights(spec).copy()
+    wr[[e for e in range(spec.E) if e != 3]] = np.nan
+    experts = {3: synth.expert(spec, 3)}
+    r2 = oracle.layer(x, wr, None, 2, experts)
+    r1 = oracle.layer(x, wr, None, 1, experts)
+    assert (r2["ids"][:, 0] == 3).all() and (r2["ids"][:, 1] == NO_EXPERT).all()
+    assert (r2["w"][:, 0] == 1.0).all() and (r2["w"][:, 1] == 0.0).all()
+    assert not r2["h"][1::2].any() and not r2["y"][1::2].any()
+    assert np.array_equal(r2["out"], r1["out"])
+    assert np.isfinite(r2["out"]).all()
+
+
 # --------------------------------------------------------------- sorter
 
 @pytest.mark.parametrize("T,k,E", [(1, 6, 256), (16, 6, 256), (37, 2, 8), (64, 6, 256)])
