@@ -24,14 +24,24 @@ moe_status ensure_smem_attr(const void *kern, int bytes, const char *name);
 
 // Tensor-core path of the expert projections (tc_expert.cu): mode 0 gate/up
 // with SwiGLU into out0, 1 gate into out0 and up into out1, 2 down into out0.
-// Used by the stage calls for batches of more than kTensorMinRows - 1 rows.
+// Tile policy of the stage calls ("Optimizing DeepSeek V4 Flash Inference on
+// a Strix Halo Pair", "MXFP4 routed-expert kernels": a direct route for small
+// batches instead of partially filled expert tiles): a call of fewer than
+// kTensorMinRows rows runs every expert on the CUDA-core kernel (the exact-
+// rows range); a larger call splits its experts on the device by their row
+// counts in `offsets`: at most kLightExpertRows rows on the CUDA-core kernel,
+// more on the tensor-core kernel, in two launches on disjoint experts.
 constexpr int kTensorMinRows = 17;
+#ifndef MOE_LIGHT_EXPERT_ROWS
+#define MOE_LIGHT_EXPERT_ROWS 4
+#endif
+constexpr int kLightExpertRows = MOE_LIGHT_EXPERT_ROWS;
 bool tc_expert_supported(int K, int N);
 moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
                             const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
                             const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E,
-                            int K, int N, int bytoken, float *out0, float *out1, int64_t ld_out, cudaStream_t stream,
-                            const char *name);
+                            int K, int N, int bytoken, int min_rows, float *out0, float *out1, int64_t ld_out,
+                            cudaStream_t stream, const char *name);
 
 // The single-launch decode forward (decode.cu) behind moe_decode_forward and
 // moe_decode_forward_shared: their arguments, the shared expert's (sh, or

@@ -53,21 +53,34 @@ struct MxArgs {
   uint32_t wreg;      // bytes of one matrix's weight slice region in a stage
   uint32_t sreg;      // bytes of one matrix's scale slice region (16-aligned)
   int scale16;        // scale rows are whole 16-byte chunks at 16-byte aligned addresses
-  int rowtab;         // sorted positions (<= kRowTab) get their activation row from shared memory
+  int rowtab;         // sorted positions (< cap <= kRowTab) get their activation row from shared memory
   int act_smem;       // all activation rows are staged in shared memory
+  int win_rows;       // else (if > 0): the rows of each expert are staged in passes of this many (two buffers)
+  int max_rows;       // experts with more rows than this are left to the tensor-core kernel
   uint32_t act_row_bytes;  // K codes (two half-block planes) + nb scales + nb block sums
   unsigned *status;
 };
 
 constexpr int kRowTab = 4096;
+// Activation rows per pass when not every row fits shared memory (two
+// buffers of this many rows; what is left of shared memory goes to the ring).
+#ifndef MOE_WIN_ROWS
+#define MOE_WIN_ROWS 8
+#endif
+constexpr int kWinRows = MOE_WIN_ROWS;
 
 // Shared-memory layout (dynamic):
 //   [nstage weight stages][full bars][empty bars][active: E][offs: E+1]
-//   [rowtab: kRowTab ints, if used][activation rows, if staged]
+//   [rowtab: cap ints, if used][activation rows: all of them, or a window]
 // An activation row holds the K Q8 codes as two planes of 16-byte half
 // blocks (first halves of all blocks, then second halves: lanes reading
 // consecutive blocks hit consecutive 16-byte bank groups), then nb fp32
-// scales, then nb int32 block sums.
+// scales, then nb int32 block sums.  When not every activation row fits,
+// the rows of each expert are taken in passes of at most win_rows rows, in
+// two window buffers: the rows of pass i+1 are copied (cp.async) while pass
+// i is computed, and each thread adds the block sums of the blocks it
+// copied once its copies have landed; one barrier per pass hands both
+// buffers over.
 template <int MODE, int S>
 __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   constexpr int NM = (MODE == kDown) ? 1 : 2;
@@ -87,8 +100,8 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   uint64_t *empty = full + nstage;
   int *active = reinterpret_cast<int *>(empty + nstage);  // [E] active experts, in id order
   int *offs = active + p.E;                               // [E+1] copy of offsets
-  int *rowtab = offs + p.E + 1;                           // [kRowTab] activation row per sorted position
-  uint8_t *act = reinterpret_cast<uint8_t *>(rowtab + (p.rowtab ? kRowTab : 0));
+  int *rowtab = offs + p.E + 1;                           // [cap] activation row per sorted position
+  uint8_t *act = reinterpret_cast<uint8_t *>(rowtab + (p.rowtab ? p.cap : 0));
   act = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(act) + 15) & ~uintptr_t(15));
   const uint32_t act_base = smem_addr(act);
 
@@ -113,7 +126,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
         const int64_t b = offs[e], en = offs[e + 1];
         const bool bad = b < 0 || en < b || en > p.cap;
         if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-        act_e = !bad && en > b;
+        act_e = !bad && en > b && en - b <= p.max_rows;  // heavier experts: the tensor-core kernel
       }
       const unsigned m = __ballot_sync(0xffffffffu, act_e);
       if (act_e) active[cnt + __popc(m & lt)] = e;
@@ -165,9 +178,11 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   // -------------------------------------------------------------- consumers
   // Activation row of each sorted position (-1: padding, -2: out of range).
   const int nsorted = offs[p.E] < 0 ? 0 : (offs[p.E] > p.cap ? (int)p.cap : offs[p.E]);
+  // (positions past offsets[E] hold no entry: -2, so that malformed offsets
+  // can never turn an unwritten entry into a row index)
   if (p.rowtab) {
-    for (int q = tid; q < nsorted; q += ncons * 32) {
-      const int a = p.sorted[q];
+    for (int q = tid; q < p.cap; q += ncons * 32) {
+      const int a = q < nsorted ? p.sorted[q] : p.A;
       rowtab[q] = a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : token_of(a, p.kdiv)));
     }
   }
@@ -182,60 +197,118 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   }
   bar_sync_named(1, ncons * 32);
 
+  // activation row of sorted position q (-1: padding, -2: out of range)
+  auto row_of = [&](int q) -> int {
+    if (p.rowtab) return rowtab[q];
+    const int a = p.sorted[q];
+    return a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : token_of(a, p.kdiv)));
+  };
+  const bool win = !p.act_smem && p.win_rows > 0;
+  const int W = win ? p.win_rows : 1 << 30;
+  const uint32_t wbuf = (uint32_t)W * p.act_row_bytes;  // bytes of one window buffer
+  // the passes, in ring order: pass (it, c0) takes rows [c0, min(c0 + W, seg_e)) of item it
+  auto next_pass = [&](int &it, int &c0) {
+    const int e = active[it];
+    c0 += W;
+    if (c0 >= offs[e + 1]) {
+      ++it;
+      c0 = it < nact ? offs[active[it]] : 0;
+    }
+  };
+  // copies of the rows of pass (it, c0) into window buffer `buf` (no wait)
+  auto copy_pass = [&](int it, int c0, int buf) {
+    const int c1 = min(offs[active[it] + 1], c0 + W);
+    const uint32_t base = act_base + (uint32_t)buf * wbuf;
+    for (int idx = tid; idx < (c1 - c0) * nb; idx += ncons * 32) {
+      const int qq = idx / nb, b = idx - qq * nb;
+      const int arow = row_of(c0 + qq);
+      if (arow < 0) continue;
+      const uint32_t row = base + (uint32_t)qq * p.act_row_bytes;
+      const int8_t *src = p.aq + (int64_t)arow * p.ld_aq + 32 * b;
+      cp_async16(row + 16u * b, src);
+      cp_async16(row + 16u * (nb + b), src + 16);
+      cp_async4(row + (uint32_t)p.K + 4u * b, p.as + (int64_t)arow * p.ld_as + b);
+    }
+    cp_async_commit();
+  };
+  // block sums of the blocks this thread copied for pass (it, c0)
+  auto sum_pass = [&](int it, int c0, int buf) {
+    const int c1 = min(offs[active[it] + 1], c0 + W);
+    const uint32_t base = act_base + (uint32_t)buf * wbuf;
+    for (int idx = tid; idx < (c1 - c0) * nb; idx += ncons * 32) {
+      const int qq = idx / nb, b = idx - qq * nb;
+      if (row_of(c0 + qq) < 0) continue;
+      const uint32_t row = base + (uint32_t)qq * p.act_row_bytes;
+      sts32(row + (uint32_t)p.K + 4u * (nb + b), (uint32_t)block_sum8(lds128(row + 16u * b), lds128(row + 16u * (nb + b))));
+    }
+  };
+  int pit = 0, pc0 = nact > 0 ? offs[active[0]] : 0, pbuf = 0;  // the pass whose rows are being copied
+  if (win && nact > 0) copy_pass(pit, pc0, pbuf);
+
+  // A warp whose wait on a stage gave up stops computing, but keeps arriving
+  // on the ring and on the named barriers, so no other warp waits on it.
+  bool dead = false;
   for (int it = 0; it < nact; ++it) {
     const int st = it % nstage;
-    if (!mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status)) break;
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
     const int e = active[it];
     const int seg_b = offs[e], seg_e = offs[e + 1];
     const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
-
-    for (int r = warp; r < R; r += ncons) {
-      uint32_t wq[NM][S][8];
-      float ws[NM][S];
-      load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
-      const int n = n0 + r;
+    for (int c0 = seg_b; c0 < seg_e; c0 += W) {  // passes over the expert's rows
+      const int c1 = min(seg_e, c0 + W);
+      uint32_t wrows = act_base;  // window buffer of this pass
+      if (win) {
+        // this pass's rows (pit, pc0 == it, c0): wait for this thread's
+        // copies, add their block sums, then one barrier: every row of the
+        // pass is ready and every warp is done with the other buffer
+        cp_async_wait<0>();
+        sum_pass(pit, pc0, pbuf);
+        wrows = act_base + (uint32_t)pbuf * wbuf;
+        bar_sync_named(1, ncons * 32);
+        next_pass(pit, pc0);
+        pbuf ^= 1;
+        if (pit < nact) copy_pass(pit, pc0, pbuf);  // the next pass's rows, while this one is computed
+      }
+      if (dead) continue;
+      for (int r = warp; r < R; r += ncons) {
+        uint32_t wq[NM][S][8];
+        float ws[NM][S];
+        load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
+        const int n = n0 + r;
 #pragma unroll 1
-      for (int q = seg_b; q < seg_e; ++q) {
-        int a, arow;
-        if (p.rowtab && q < kRowTab) {
-          arow = rowtab[q];
+        for (int q = c0; q < c1; ++q) {
+          const int arow = row_of(q);
           if (arow < 0) {
             if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
             continue;
           }
-          a = p.sorted[q];
-        } else {
-          a = p.sorted[q];
-          if (a < 0) continue;
-          if (a >= p.A) {
-            if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-            continue;
-          }
-          arow = MODE == kDown ? a : token_of(a, p.kdiv);
-        }
-        float acc[NM];
-        if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
-        else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
-        if (NM == 2) {
-          float g, u;
-          reduce_pair(acc[0], acc[NM - 1], g, u);
-          if (lane == 0) {
-            if (MODE == kGateUpSwiglu) {
-              p.out0[(int64_t)a * p.ld_out + n] = __fmul_rn(silu(g), u);
-            } else {
-              p.out0[(int64_t)a * p.ld_out + n] = g;
-              p.out1[(int64_t)a * p.ld_out + n] = u;
+          const int a = p.sorted[q];
+          float acc[NM];
+          if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+          else if (win) row_dot_smem<NM, S>(wrows + (uint32_t)(q - c0) * p.act_row_bytes, p.K, wq, ws, acc);
+          else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+          if (NM == 2) {
+            float g, u;
+            reduce_pair(acc[0], acc[NM - 1], g, u);
+            if (lane == 0) {
+              if (MODE == kGateUpSwiglu) {
+                p.out0[(int64_t)a * p.ld_out + n] = __fmul_rn(silu(g), u);
+              } else {
+                p.out0[(int64_t)a * p.ld_out + n] = g;
+                p.out1[(int64_t)a * p.ld_out + n] = u;
+              }
             }
+          } else {
+            const float v = reduce_one(acc[0]);
+            if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
           }
-        } else {
-          const float v = reduce_one(acc[0]);
-          if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
+  cp_async_wait<0>();  // nothing of this thread's in flight at exit
 }
 
 template <int MODE>
@@ -253,7 +326,7 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   const int sms = sm_count();
   p.rowtab = p.cap <= kRowTab ? 1 : 0;
   p.act_row_bytes = (uint32_t)p.K + 8u * nb;
-  const size_t fixed = (size_t)p.E * 8 + 4 + 16 * 8 + 32 + (p.rowtab ? 4 * kRowTab : 0);
+  const size_t fixed = (size_t)p.E * 8 + 4 + 16 * 8 + 32 + (p.rowtab ? 4 * (size_t)p.cap : 0) + 16;
   int G = p.N < sms ? p.N : sms;
   for (;;) {
     p.R = (p.N + G - 1) / G;
@@ -263,16 +336,26 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
     if (budget >= fixed + 2 * (size_t)p.stage_bytes || G >= p.N) break;
     G = (2 * G < p.N) ? 2 * G : p.N;
   }
-  const size_t act_bytes = (size_t)p.n_act * p.act_row_bytes + 16;
-  p.act_smem = budget >= fixed + 2 * (size_t)p.stage_bytes + act_bytes ? 1 : 0;
-  const size_t avail = budget - fixed - (p.act_smem ? act_bytes : 0);
+  if (budget < fixed + 2 * (size_t)p.stage_bytes)
+    return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
+  // every activation row in shared memory if they fit beside a two-stage
+  // ring; else two window buffers of up to kWinRows rows each
+  const size_t room = budget - fixed - 2 * (size_t)p.stage_bytes;
+  size_t act_bytes = (size_t)p.n_act * p.act_row_bytes;
+  p.act_smem = act_bytes <= room ? 1 : 0;
+  p.win_rows = 0;
+  if (!p.act_smem) {
+    const size_t w = room / (2 * (size_t)p.act_row_bytes);
+    p.win_rows = (int)(w < (size_t)kWinRows ? w : (size_t)kWinRows);
+    act_bytes = 2 * (size_t)p.win_rows * p.act_row_bytes;
+  }
+  const size_t avail = budget - fixed - act_bytes;
   int ns = (int)(avail / p.stage_bytes);
   p.nstage = ns > 6 ? 6 : ns;
-  if (p.nstage < 2) return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
   p.scale16 = (nb % 16) == 0 && (uintptr_t)p.s0 % 16 == 0 && (p.s1 == nullptr || (uintptr_t)p.s1 % 16 == 0);
   const int per_warp = (p.R + 14) / 15;
   const int ncons = (p.R + per_warp - 1) / per_warp;
-  const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + (p.act_smem ? act_bytes : 0);
+  const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + act_bytes;
   const dim3 block((ncons + 1) * 32);
 
   auto kern = S == 1 ? mx_expert_kernel<MODE, 1> : (S == 2 ? mx_expert_kernel<MODE, 2> : mx_expert_kernel<MODE, 4>);
@@ -322,10 +405,17 @@ static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const f
   if (ld < I) return fail(MOE_ERR_INVALID_ARG, "%s: output ld=%lld < I=%d", name, (long long)ld, I);
   if (mode == kGateUpRaw && (!o1 || (uintptr_t)o1 % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: bad up output", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (T >= kTensorMinRows && tc_expert_supported(H, I))
-    return launch_tc_expert(mode == kGateUpSwiglu ? 0 : 1, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap,
-                            T * k, k, E, H, I, 1, o0, mode == kGateUpSwiglu ? nullptr : o1, ld, s, name);
+  // tile policy: from kTensorMinRows rows on, experts with more than
+  // kLightExpertRows rows take the tensor-core kernel, the rest this one
+  const bool split = T >= kTensorMinRows && tc_expert_supported(H, I);
+  if (split) {
+    st = launch_tc_expert(mode == kGateUpSwiglu ? 0 : 1, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap,
+                          T * k, k, E, H, I, 1, kLightExpertRows, o0, mode == kGateUpSwiglu ? nullptr : o1, ld, s,
+                          name);
+    if (st != MOE_OK) return st;
+  }
   MxArgs p{};
+  p.max_rows = split ? kLightExpertRows : 0x7fffffff;
   p.aq = xq; p.ld_aq = ld_xq; p.as = xs; p.ld_as = ld_xs;
   p.w0 = wg; p.s0 = sg; p.w1 = wu; p.s1 = su;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
@@ -363,10 +453,14 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
                                H, I, y, ld_y, I, T * k);
   if (st != MOE_OK || T == 0) return st;
   if (ld_y < H) return fail(MOE_ERR_INVALID_ARG, "%s: ld_y=%lld < H=%d", name, (long long)ld_y, H);
-  if (T >= kTensorMinRows && tc_expert_supported(I, H))
-    return launch_tc_expert(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T * k, k, E, I,
-                            H, 0, y, nullptr, ld_y, static_cast<cudaStream_t>(stream), name);
+  const bool split = T >= kTensorMinRows && tc_expert_supported(I, H);  // tile policy, as for gate/up
+  if (split) {
+    st = launch_tc_expert(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T * k, k, E, I, H,
+                          0, kLightExpertRows, y, nullptr, ld_y, static_cast<cudaStream_t>(stream), name);
+    if (st != MOE_OK) return st;
+  }
   MxArgs p{};
+  p.max_rows = split ? kLightExpertRows : 0x7fffffff;
   p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
   p.w0 = wd; p.s0 = sd;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;

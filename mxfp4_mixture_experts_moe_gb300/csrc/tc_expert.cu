@@ -109,6 +109,7 @@ struct TcArgs {
   int64_t cap;
   int A, k, E, K, N;  // K reduction length, N output rows per expert
   int bytoken;        // activation row of assignment a: a / k (1) or a (0)
+  int min_rows;       // experts with at most this many rows are left to the CUDA-core kernel
   uint32_t kdiv;
   float *out0, *out1;
   int64_t ld_out;
@@ -244,31 +245,6 @@ MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   return tl;
 }
 
-// The drain's K-step for a warp whose rows hold an E8M0 byte outside the
-// MMA's clamp range: acc = fma(D, xs * 2^(u - uc), acc) per matrix, block and
-// column, D = I_b 2^(uc-128).  A separate, never-inlined function, so that
-// the rare case costs the common one no registers.  sb: offset of the
-// K-step's two bytes in this row's E8M0 bytes of each matrix.
-template <int NM>
-__device__ __noinline__ void drain_remainders(float (&acc)[NM][16], uint32_t dcol, const float (&x0)[16],
-                                              const float (&x1)[16], const uint8_t *s0, const uint8_t *s1,
-                                              int64_t sb) {
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-    const uint32_t w2 = __ldg(reinterpret_cast<const unsigned short *>((m == 0 ? s0 : s1) + sb));
-    const float f0 = e8m0_remainder(w2 & 0xFFu), f1 = e8m0_remainder((w2 >> 8) & 0xFFu);
-    uint32_t de[16], dd[16];
-    tmem_ld16_nowait(dcol + (uint32_t)m * kN, de);
-    tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd);
-    tmem_ld_wait();
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      acc[m][c] = __fmaf_rn(__uint_as_float(de[c]), __fmul_rn(x0[c], f0), acc[m][c]);
-      acc[m][c] = __fmaf_rn(__uint_as_float(dd[c]), __fmul_rn(x1[c], f1), acc[m][c]);
-    }
-  }
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, const __grid_constant__ TcMaps maps) {
   constexpr int NM = MODE == kDownMode ? 1 : 2;
@@ -326,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         const int b = p.offsets[e], en = p.offsets[e + 1];
         const bool bad = b < 0 || en < b || en > p.cap;
         if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-        if (!bad && en > b) nt = ((en - b + kNT - 1) / kNT) * mt;
+        if (!bad && en - b > p.min_rows) nt = ((en - b + kNT - 1) / kNT) * mt;
       }
       int incl = nt;
 #pragma unroll
@@ -396,23 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
           tc_fence_after();
           if (active) {
             const uint32_t dcol = tmem + lanes + kDBase + (uint32_t)db * NM * kN + 16u * h;
-            // scales of blocks 8 st + 2 s and + 1 of columns 16 h .. 16 h + 15
-            float x0[16], x1[16];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 a = lds128(xsb + (uint32_t)((2 * s) * kNT + 16 * h + 4 * v) * 4u);
-              const uint4 b = lds128(xsb + (uint32_t)((2 * s + 1) * kNT + 16 * h + 4 * v) * 4u);
-              x0[4 * v] = __uint_as_float(a.x); x0[4 * v + 1] = __uint_as_float(a.y);
-              x0[4 * v + 2] = __uint_as_float(a.z); x0[4 * v + 3] = __uint_as_float(a.w);
-              x1[4 * v] = __uint_as_float(b.x); x1[4 * v + 1] = __uint_as_float(b.y);
-              x1[4 * v + 2] = __uint_as_float(b.z); x1[4 * v + 3] = __uint_as_float(b.w);
-            }
             if (!ext) {
               uint32_t de[NM][16], dd[NM][16];
 #pragma unroll
               for (int m = 0; m < NM; ++m) {
                 tmem_ld16_nowait(dcol + (uint32_t)m * kN, de[m]);
                 tmem_ld16_nowait(dcol + (uint32_t)m * kN + kNT, dd[m]);
+              }
+              // scales of blocks 8 st + 2 s and + 1 of columns 16 h .. 16 h + 15
+              float x0[16], x1[16];
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint4 a = lds128(xsb + (uint32_t)((2 * s) * kNT + 16 * h + 4 * v) * 4u);
+                const uint4 b = lds128(xsb + (uint32_t)((2 * s + 1) * kNT + 16 * h + 4 * v) * 4u);
+                x0[4 * v] = __uint_as_float(a.x); x0[4 * v + 1] = __uint_as_float(a.y);
+                x0[4 * v + 2] = __uint_as_float(a.z); x0[4 * v + 3] = __uint_as_float(a.w);
+                x1[4 * v] = __uint_as_float(b.x); x1[4 * v + 1] = __uint_as_float(b.y);
+                x1[4 * v + 2] = __uint_as_float(b.z); x1[4 * v + 3] = __uint_as_float(b.w);
               }
               tmem_ld_wait();
 #pragma unroll
@@ -424,7 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
                 }
               }
             } else {
-              drain_remainders<NM>(acc, dcol, x0, x1, p.s0, p.s1, (S.wrow[tb] + r) * (int64_t)(K / 32) + st * 8 + 2 * s);
+              // a byte of this quadrant's rows lay outside the MMA's clamp
+              // range: D = I_b 2^(uc-128) times xs 2^(u-uc), one matrix and
+              // one block at a time (the activation scales read again from
+              // shared memory, so this rare path needs few registers)
+#pragma unroll
+              for (int m = 0; m < NM; ++m) {
+                const int64_t sb = (S.wrow[tb] + r) * (int64_t)(K / 32) + st * 8 + 2 * s;
+                const uint32_t w2 = __ldg(reinterpret_cast<const unsigned short *>((m == 0 ? p.s0 : p.s1) + sb));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                  const float f = e8m0_remainder((w2 >> (8 * half)) & 0xFFu);
+                  uint32_t d[16];
+                  tmem_ld16_nowait(dcol + (uint32_t)(m * kN + half * kNT), d);
+                  tmem_ld_wait();
+                  const uint32_t xrow = xsb + (uint32_t)((2 * s + half) * kNT + 16 * h) * 4u;
+#pragma unroll
+                  for (int c = 0; c < 16; ++c)
+                    acc[m][c] = __fmaf_rn(__uint_as_float(d[c]), __fmul_rn(lds_f32(xrow + 4u * c), f), acc[m][c]);
+                }
+              }
             }
           }
           {
@@ -721,13 +716,14 @@ bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t col
 bool tc_expert_supported(int K, int N) { return K % kStageK == 0 && K <= 8192 && N % kRows == 0; }
 
 // Launch of the tensor-core path (moe_mxfp4_gateup_swiglu, moe_mxfp4_gateup
-// and moe_mxfp4_down for T > 16).  mode 0: gate and up with SwiGLU into out0;
-// 1: gate into out0, up into out1; 2: down into out0.
+// and moe_mxfp4_down for T > 16) over the experts with more than min_rows
+// rows.  mode 0: gate and up with SwiGLU into out0; 1: gate into out0, up
+// into out1; 2: down into out0.
 moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as,
                             const uint8_t *w0, const uint8_t *s0, const uint8_t *w1, const uint8_t *s1,
                             const int32_t *offsets, const int32_t *sorted, int64_t cap, int A, int k, int E, int K,
-                            int N, int bytoken, float *out0, float *out1, int64_t ld_out, cudaStream_t stream,
-                            const char *name) {
+                            int N, int bytoken, int min_rows, float *out0, float *out1, int64_t ld_out,
+                            cudaStream_t stream, const char *name) {
   if (!tc_expert_supported(K, N))
     return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs K %% 256 == 0 (<= 8192) and rows %% 128 == 0", name);
   if (E > 4096) return fail(MOE_ERR_UNSUPPORTED, "%s: E=%d", name, E);
@@ -743,7 +739,7 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
   p.aq = aq; p.ld_aq = ld_aq; p.as = as; p.ld_as = ld_as;
   p.s0 = s0; p.s1 = s1;
   p.offsets = offsets; p.sorted = sorted; p.cap = cap;
-  p.A = A; p.k = k; p.E = E; p.K = K; p.N = N; p.bytoken = bytoken;
+  p.A = A; p.k = k; p.E = E; p.K = K; p.N = N; p.bytoken = bytoken; p.min_rows = min_rows < 0 ? 0 : min_rows;
   p.kdiv = kdiv_of(k);
   p.out0 = out0; p.out1 = out1; p.ld_out = ld_out;
   p.status = device_status_word();

@@ -205,6 +205,11 @@ class MoeLayer:
                 return 1
             return 1 + 5  # the shared expert's quant x, gate/up, quant h, down, join
         n = 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
-        if self.lw.shared is not None:
+        lw = self.lw
+        if T >= 17:  # tile policy: light experts on the CUDA-core kernel, the rest on the tensor-core kernel
+            n += (lw.H % 256 == 0 and lw.I % 128 == 0) + (lw.I % 256 == 0 and lw.H % 128 == 0)
+        if lw.shared is not None:
             n += 4  # the shared expert's gate/up, quant h, down, join
+            if T >= 17:
+                n += (lw.H % 256 == 0 and lw.I % 128 == 0) + (lw.I % 256 == 0 and lw.H % 128 == 0)
         return n
