@@ -99,9 +99,9 @@ MOE_API const char *moe_last_error(void);
 
 /* ABI version of this header (bumped on any signature change or addition;
  * 2 adds moe_join_add, moe_decode_max_tokens_shared and
- * moe_decode_forward_shared). */
+ * moe_decode_forward_shared; 3 adds moe_mxf4_mma_probe). */
 MOE_API int moe_abi_version(void);
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device into *flags (may be NULL).  Returns MOE_ERR_DEVICE when the
@@ -349,6 +349,21 @@ MOE_API moe_status moe_decode_forward_noalloc(const void *x, moe_dtype x_dtype, 
                                               const uint8_t *su, const uint8_t *wd, const uint8_t *sd,
                                               int T, int H, int E, int k, int I,
                                               float *out, int64_t ld_out, void *stream);
+
+/* ---------------------------------------------------------------- measurement */
+
+/* Throughput probe of the tensor-core instruction the prefill projections
+ * run on (a measurement aid beside the layer; the pages have no counterpart:
+ * it measures the roofline the tensor-core expert path is reported against).
+ * One CTA per SM issues `iters` accumulating block-scaled FP4 MMAs (kind::mxf4
+ * with E8M0 block scales, M = 128, N = n, K = 64) on zeroed shared-memory
+ * operands, in the operand and scale layout of the tensor-core expert kernel.
+ * *flops receives the launch's floating-point operations,
+ * 2 * 128 * n * 64 * iters * (number of SMs); the caller times the launch
+ * (events on `stream`).  n: 64, 128 or 256; 1 <= iters <= 2^20 (else
+ * MOE_ERR_INVALID_ARG, nothing launched).  A wait that runs out raises
+ * MOE_DEV_WAIT_TIMEOUT. */
+MOE_API moe_status moe_mxf4_mma_probe(int n, int iters, double *flops, void *stream);
 
 #ifdef __cplusplus
 }

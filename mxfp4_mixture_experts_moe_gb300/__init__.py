@@ -29,7 +29,7 @@ EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
            "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_join_add", "moe_decode_workspace_bytes",
            "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc",
-           "moe_decode_max_tokens_shared", "moe_decode_forward_shared"]
+           "moe_decode_max_tokens_shared", "moe_decode_forward_shared", "moe_mxf4_mma_probe"]
 
 _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 _SIG = {
@@ -51,6 +51,7 @@ _SIG = {
                            + [_P, _L, _P, _L, _P, C.c_size_t, _P]),
     "moe_decode_forward_noalloc": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 6 + [_I] * 5 + [_P, _L, _P]),
     "moe_decode_max_tokens_shared": (_I, [_I, _I, _I, _I]),
+    "moe_mxf4_mma_probe": (_I, [_I, _I, C.POINTER(C.c_double), _P]),
     "moe_decode_forward_shared": (_I, [_P, _I, _L, _P, _I, _P] + [_P] * 12 + [_I] * 5 + [_P, _L] + [_P] * 3
                                   + [_P, _L, _P, _L, _P, _L, _P, _L, _P, C.c_size_t, _P]),
 }
@@ -58,29 +59,34 @@ library_path = _LIB_PATH
 
 
 class _Native:
-    """The loaded C library; loads on first attribute access, raises if absent."""
+    """The loaded C library; loads on first attribute access, raises if absent.
+    Each entry point gets its C signature when it is first used."""
     _cdll = None
+    _bound = set()
 
     def __getattr__(self, name):
         if _Native._cdll is None:
             if not os.path.exists(_LIB_PATH):
                 raise ImportError(f"{_LIB_PATH} is missing: build it with "
                                   "`python -m mxfp4_mixture_experts_moe_gb300.build` (there is no fallback path)")
-            lib = C.CDLL(_LIB_PATH)
-            for fname, (res, args) in _SIG.items():
-                f = getattr(lib, fname)
-                f.restype = res
-                f.argtypes = args
-            _Native._cdll = lib
-        return getattr(_Native._cdll, name)
+            _Native._cdll = C.CDLL(_LIB_PATH)
+        f = getattr(_Native._cdll, name)
+        if name not in _Native._bound and name in _SIG:
+            f.restype, f.argtypes = _SIG[name]
+            _Native._bound.add(name)
+        return f
 
 
 _lib = _Native()
 
 
 def load():
-    """Load the library now (raises ImportError if it has not been built)."""
+    """Load the library now (raises ImportError if it has not been built) and
+    give every entry point it exports its C signature."""
     _lib.moe_abi_version
+    for name in _SIG:
+        if hasattr(_Native._cdll, name):
+            getattr(_lib, name)
     return _Native._cdll
 
 
@@ -250,3 +256,12 @@ def moe_decode_forward_noalloc(x, w_router, bias, wg, sg, wu, su, wd, sd, k, out
 
 
 from .layer import MoeLayer, LayerWeights, SharedExpertWeights, Workspace  # noqa: E402
+
+
+def moe_mxf4_mma_probe(n: int, iters: int, stream=None) -> float:
+    """Launch the FP4 tensor-core throughput probe (one CTA per SM, `iters`
+    M=128 x N=n x K=64 block-scaled MMAs each); returns the launch's flops.
+    The caller times the launch (events on the same stream)."""
+    flops = C.c_double(0.0)
+    _check(_lib.moe_mxf4_mma_probe(int(n), int(iters), C.byref(flops), _stream(stream)))
+    return flops.value

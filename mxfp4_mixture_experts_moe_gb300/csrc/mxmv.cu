@@ -81,7 +81,10 @@ constexpr int kWinRows = MOE_WIN_ROWS;
 // i is computed, and each thread adds the block sums of the blocks it
 // copied once its copies have landed; one barrier per pass hands both
 // buffers over.
-template <int MODE, int S>
+// WIN: the activation rows of each expert are staged in window passes (a
+// separate instantiation, so the kernel of the other cases keeps its own
+// tight loop).
+template <int MODE, int S, bool WIN>
 __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   constexpr int NM = (MODE == kDown) ? 1 : 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -197,14 +200,70 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   }
   bar_sync_named(1, ncons * 32);
 
+  if constexpr (!WIN) {
+    for (int it = 0; it < nact; ++it) {
+      const int st = it % nstage;
+      if (!mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status)) break;
+      const int e = active[it];
+      const int seg_b = offs[e], seg_e = offs[e + 1];
+      const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
+
+      for (int r = warp; r < R; r += ncons) {
+        uint32_t wq[NM][S][8];
+        float ws[NM][S];
+        load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
+        const int n = n0 + r;
+#pragma unroll 1
+        for (int q = seg_b; q < seg_e; ++q) {
+          int a, arow;
+          if (p.rowtab) {
+            arow = rowtab[q];
+            if (arow < 0) {
+              if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+              continue;
+            }
+            a = p.sorted[q];
+          } else {
+            a = p.sorted[q];
+            if (a < 0) continue;
+            if (a >= p.A) {
+              if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+              continue;
+            }
+            arow = MODE == kDown ? a : token_of(a, p.kdiv);
+          }
+          float acc[NM];
+          if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+          else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+          if (NM == 2) {
+            float g, u;
+            reduce_pair(acc[0], acc[NM - 1], g, u);
+            if (lane == 0) {
+              if (MODE == kGateUpSwiglu) {
+                p.out0[(int64_t)a * p.ld_out + n] = __fmul_rn(silu(g), u);
+              } else {
+                p.out0[(int64_t)a * p.ld_out + n] = g;
+                p.out1[(int64_t)a * p.ld_out + n] = u;
+              }
+            }
+          } else {
+            const float v = reduce_one(acc[0]);
+            if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+    }
+    return;
+  } else {
   // activation row of sorted position q (-1: padding, -2: out of range)
   auto row_of = [&](int q) -> int {
     if (p.rowtab) return rowtab[q];
     const int a = p.sorted[q];
     return a < 0 ? -1 : (a >= p.A ? -2 : (MODE == kDown ? a : token_of(a, p.kdiv)));
   };
-  const bool win = !p.act_smem && p.win_rows > 0;
-  const int W = win ? p.win_rows : 1 << 30;
+  const int W = p.win_rows;
   const uint32_t wbuf = (uint32_t)W * p.act_row_bytes;  // bytes of one window buffer
   // the passes, in ring order: pass (it, c0) takes rows [c0, min(c0 + W, seg_e)) of item it
   auto next_pass = [&](int &it, int &c0) {
@@ -243,7 +302,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
     }
   };
   int pit = 0, pc0 = nact > 0 ? offs[active[0]] : 0, pbuf = 0;  // the pass whose rows are being copied
-  if (win && nact > 0) copy_pass(pit, pc0, pbuf);
+  if (nact > 0) copy_pass(pit, pc0, pbuf);
 
   // A warp whose wait on a stage gave up stops computing, but keeps arriving
   // on the ring and on the named barriers, so no other warp waits on it.
@@ -256,19 +315,16 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
     const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
     for (int c0 = seg_b; c0 < seg_e; c0 += W) {  // passes over the expert's rows
       const int c1 = min(seg_e, c0 + W);
-      uint32_t wrows = act_base;  // window buffer of this pass
-      if (win) {
-        // this pass's rows (pit, pc0 == it, c0): wait for this thread's
-        // copies, add their block sums, then one barrier: every row of the
-        // pass is ready and every warp is done with the other buffer
-        cp_async_wait<0>();
-        sum_pass(pit, pc0, pbuf);
-        wrows = act_base + (uint32_t)pbuf * wbuf;
-        bar_sync_named(1, ncons * 32);
-        next_pass(pit, pc0);
-        pbuf ^= 1;
-        if (pit < nact) copy_pass(pit, pc0, pbuf);  // the next pass's rows, while this one is computed
-      }
+      // this pass's rows (pit, pc0 == it, c0): wait for this thread's
+      // copies, add their block sums, then one barrier: every row of the
+      // pass is ready and every warp is done with the other buffer
+      cp_async_wait<0>();
+      sum_pass(pit, pc0, pbuf);
+      const uint32_t wrows = act_base + (uint32_t)pbuf * wbuf;
+      bar_sync_named(1, ncons * 32);
+      next_pass(pit, pc0);
+      pbuf ^= 1;
+      if (pit < nact) copy_pass(pit, pc0, pbuf);  // the next pass's rows, while this one is computed
       if (dead) continue;
       for (int r = warp; r < R; r += ncons) {
         uint32_t wq[NM][S][8];
@@ -284,9 +340,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
           }
           const int a = p.sorted[q];
           float acc[NM];
-          if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
-          else if (win) row_dot_smem<NM, S>(wrows + (uint32_t)(q - c0) * p.act_row_bytes, p.K, wq, ws, acc);
-          else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+          row_dot_smem<NM, S>(wrows + (uint32_t)(q - c0) * p.act_row_bytes, p.K, wq, ws, acc);
           if (NM == 2) {
             float g, u;
             reduce_pair(acc[0], acc[NM - 1], g, u);
@@ -309,6 +363,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
   cp_async_wait<0>();  // nothing of this thread's in flight at exit
+  }
 }
 
 template <int MODE>
@@ -339,26 +394,36 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   if (budget < fixed + 2 * (size_t)p.stage_bytes)
     return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
   // every activation row in shared memory if they fit beside a two-stage
-  // ring; else two window buffers of up to kWinRows rows each
-  const size_t room = budget - fixed - 2 * (size_t)p.stage_bytes;
-  size_t act_bytes = (size_t)p.n_act * p.act_row_bytes;
-  p.act_smem = act_bytes <= room ? 1 : 0;
+  // ring; else, for the light experts of a large batch (the tile policy),
+  // two window buffers of up to kWinRows rows each; else rows from global
+  // memory (the 1-16-row calls: an expert has one or two rows there)
+  const size_t room = budget - fixed - 2 * (size_t)p.stage_bytes;  // >= 0: checked above
+  const size_t all_rows = (size_t)p.n_act * p.act_row_bytes;
+  size_t act_bytes = 0;  // never more than room
+  p.act_smem = all_rows <= room ? 1 : 0;
   p.win_rows = 0;
-  if (!p.act_smem) {
+  if (p.act_smem) {
+    act_bytes = all_rows;
+  } else if (p.max_rows != 0x7fffffff) {
     const size_t w = room / (2 * (size_t)p.act_row_bytes);
     p.win_rows = (int)(w < (size_t)kWinRows ? w : (size_t)kWinRows);
     act_bytes = 2 * (size_t)p.win_rows * p.act_row_bytes;
   }
-  const size_t avail = budget - fixed - act_bytes;
-  int ns = (int)(avail / p.stage_bytes);
-  p.nstage = ns > 6 ? 6 : ns;
+  const size_t ns = (budget - fixed - act_bytes) / p.stage_bytes;
+  p.nstage = ns > 6 ? 6 : (int)ns;
   p.scale16 = (nb % 16) == 0 && (uintptr_t)p.s0 % 16 == 0 && (p.s1 == nullptr || (uintptr_t)p.s1 % 16 == 0);
   const int per_warp = (p.R + 14) / 15;
   const int ncons = (p.R + per_warp - 1) / per_warp;
   const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + act_bytes;
+  if (p.nstage < 2 || smem > budget || act_bytes > room)
+    return fail(MOE_ERR_UNSUPPORTED, "%s: no shared-memory plan (stages %d, %zu bytes)", name, p.nstage, smem);
   const dim3 block((ncons + 1) * 32);
 
-  auto kern = S == 1 ? mx_expert_kernel<MODE, 1> : (S == 2 ? mx_expert_kernel<MODE, 2> : mx_expert_kernel<MODE, 4>);
+  const bool win = !p.act_smem && p.win_rows > 0;
+  auto kern = win ? (S == 1 ? mx_expert_kernel<MODE, 1, true>
+                            : (S == 2 ? mx_expert_kernel<MODE, 2, true> : mx_expert_kernel<MODE, 4, true>))
+                  : (S == 1 ? mx_expert_kernel<MODE, 1, false>
+                            : (S == 2 ? mx_expert_kernel<MODE, 2, false> : mx_expert_kernel<MODE, 4, false>));
   const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)budget, name);
   if (ast != MOE_OK) return ast;
   kern<<<G, block, smem, stream>>>(p);

@@ -41,6 +41,33 @@ MOE_DEVFN void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync
 // Generic-proxy shared-memory writes made visible to the tensor core.
 MOE_DEVFN void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Shared-memory descriptor of a 128-byte swizzled K-major tile (8-row groups
+// 1024 bytes apart), as the tensor copies of the weights lay it out.
+MOE_DEVFN uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 block scales,
+// fp32 accumulator, both operands K-major), M x N.
+MOE_DEVFN uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B with per-32 block scales from tensor memory (sfa, sfb).
+MOE_DEVFN void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                        bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+MOE_DEVFN void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // Store of 32 registers into 32 consecutive columns of this warp's 32 lanes
 // (asynchronous: tmem_st_wait() before the values are handed on).
 MOE_DEVFN void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {

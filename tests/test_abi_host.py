@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in _declared():
         assert hasattr(lib, n), n
     assert set(moe.EXPORTS) == _declared()
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
 
 
 def test_library_exports_nothing_else():
@@ -84,6 +84,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.moe_join_add(p, 32, 1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_join_add(p, 64, 1, 64, None, 64, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_join_add(p, 64, -1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
+    # tensor-core probe: unsupported n, iteration count out of range (nothing launched)
+    f = C.c_double(0.0)
+    assert lib.moe_mxf4_mma_probe(96, 16, C.byref(f), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_mxf4_mma_probe(64, 0, C.byref(f), None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_empty_batch_is_a_host_noop(lib):
