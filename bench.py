@@ -64,6 +64,7 @@ METRIC = "MoE-layer tokens/s and achieved HBM TB/s (decode 1–16 rows; prefill 
 # figure whose sources have changed since is reported as null.
 NCU_TRAFFIC = {
     # (workload, roofline kernel): (bytes per launch, source hash at capture)
+    ("decode-1", "moe_decode_forward"): (84.05e6, "10d72cae29d45403"),
 }
 # sources of each roofline kernel (the files its code comes from)
 KERNEL_SOURCES = {
