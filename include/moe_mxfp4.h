@@ -99,9 +99,10 @@ MOE_API const char *moe_last_error(void);
 
 /* ABI version of this header (bumped on any signature change or addition;
  * 2 adds moe_join_add, moe_decode_max_tokens_shared and
- * moe_decode_forward_shared; 3 adds moe_mxf4_mma_probe). */
+ * moe_decode_forward_shared; 3 adds moe_mxf4_mma_probe; 4 adds
+ * moe_mxfp4_down_combine). */
 MOE_API int moe_abi_version(void);
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device into *flags (may be NULL).  Returns MOE_ERR_DEVICE when the
@@ -213,6 +214,26 @@ MOE_API moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const float *
                           const int32_t *offsets, const int32_t *sorted, int64_t cap,
                           int T, int k, int E, int H, int I,
                           float *y, int64_t ld_y, void *stream);
+
+/* Down projection and routing-weighted combine in one pass (the down
+ * consumer of "DeepSeek-V4-Flash on AMD gfx90a", §8.2: the down outputs stay
+ * FP32 top-k partials and meet in a fixed reduction, without a round trip of
+ * y through memory).  out is bit-identical to moe_mxfp4_down followed by
+ * moe_combine on the same inputs: the same block dots and fixed fp32 order
+ * per output, then the same slot-ordered fma chain (a slot of weight exactly
+ * 0 adds nothing).
+ *  hq, hs, wd, sd, offsets, sorted, cap: as moe_mxfp4_down.
+ *  w    [T][k] fp32 routing weights (moe_route_topk's).
+ *  out  [T][ld_out] fp32 output: the layer output.
+ *  y    [T*k][ld_y] fp32: the per-slot down outputs as well, or NULL.
+ * One launch when T <= 16 and a CTA's y rows fit its shared memory; otherwise
+ * moe_mxfp4_down into y, then moe_combine (y is then required, else
+ * MOE_ERR_UNSUPPORTED).  Other requirements and errors as moe_mxfp4_down. */
+MOE_API moe_status moe_mxfp4_down_combine(const int8_t *hq, int64_t ld_hq, const float *hs, int64_t ld_hs,
+                                  const uint8_t *wd, const uint8_t *sd,
+                                  const int32_t *offsets, const int32_t *sorted, int64_t cap,
+                                  const float *w, int T, int k, int E, int H, int I,
+                                  float *out, int64_t ld_out, float *y, int64_t ld_y, void *stream);
 
 /* ---------------------------------------------------------------- combine */
 

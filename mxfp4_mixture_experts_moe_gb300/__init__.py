@@ -27,7 +27,8 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_ROW, MOE_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = ["moe_last_error", "moe_abi_version", "moe_device_status", "moe_route_topk",
            "moe_sort_tokens_capacity", "moe_sort_tokens", "act_quant_q8", "moe_mxfp4_gateup_swiglu",
-           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_combine", "moe_join_add", "moe_decode_workspace_bytes",
+           "moe_mxfp4_gateup", "moe_mxfp4_down", "moe_mxfp4_down_combine", "moe_combine", "moe_join_add",
+           "moe_decode_workspace_bytes",
            "moe_decode_max_tokens", "moe_decode_forward", "moe_decode_forward_noalloc",
            "moe_decode_max_tokens_shared", "moe_decode_forward_shared", "moe_mxf4_mma_probe"]
 
@@ -44,6 +45,7 @@ _SIG = {
     "moe_mxfp4_gateup": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _P, _L, _P]),
     "moe_mxfp4_down": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _I, _I, _P, _L, _P]),
     "moe_combine": (_I, [_P, _L, _P, _I, _I, _I, _P, _L, _P]),
+    "moe_mxfp4_down_combine": (_I, [_P, _L, _P, _L, _P, _P, _P, _P, _L, _P, _I, _I, _I, _I, _I, _P, _L, _P, _L, _P]),
     "moe_join_add": (_I, [_P, _L, _I, _I, _P, _L, _P]),
     "moe_decode_workspace_bytes": (C.c_size_t, []),
     "moe_decode_max_tokens": (_I, [_I, _I, _I, _I]),
@@ -187,6 +189,13 @@ def moe_mxfp4_down(hq, hs, wd, sd, offsets, sorted_, T, k, y, stream=None):
     E, H, I = wd.shape[0], wd.shape[1], wd.shape[2] * 2
     _check(_lib.moe_mxfp4_down(_ptr(hq), _ld(hq), _ptr(hs), _ld(hs), _ptr(wd), _ptr(sd), _ptr(offsets),
                                _ptr(sorted_), sorted_.numel(), T, k, E, H, I, _ptr(y), _ld(y), _stream(stream)))
+
+
+def moe_mxfp4_down_combine(hq, hs, wd, sd, offsets, sorted_, w, T, k, out, y=None, stream=None):
+    E, H, I = wd.shape[0], wd.shape[1], wd.shape[2] * 2
+    _check(_lib.moe_mxfp4_down_combine(_ptr(hq), _ld(hq), _ptr(hs), _ld(hs), _ptr(wd), _ptr(sd), _ptr(offsets),
+                                       _ptr(sorted_), sorted_.numel(), _ptr(w), T, k, E, H, I, _ptr(out), _ld(out),
+                                       _ptr(y), 0 if y is None else _ld(y), _stream(stream)))
 
 
 def moe_combine(y, w, out, stream=None):

@@ -47,6 +47,12 @@ struct MxArgs {
   uint32_t kdiv;      // kdiv_of(k): token of assignment a = token_of(a, kdiv)
   float *out0, *out1;
   int64_t ld_out;
+  // fused combine (down only): out[t] = slot-ordered combine of the y rows,
+  // which stay in shared memory (out0, the y rows in global memory, optional)
+  const float *wts;   // [T][k] routing weights
+  float *cout;        // [T][ld_cout] layer output
+  int64_t ld_cout;
+  int T;
   int R;              // output rows per CTA (max)
   int nstage;
   uint32_t stage_bytes;
@@ -81,10 +87,13 @@ constexpr int kWinRows = MOE_WIN_ROWS;
 // i is computed, and each thread adds the block sums of the blocks it
 // copied once its copies have landed; one barrier per pass hands both
 // buffers over.
-// WIN: the activation rows of each expert are staged in window passes (a
-// separate instantiation, so the kernel of the other cases keeps its own
-// tight loop).
-template <int MODE, int S, bool WIN>
+// WIN: the activation rows of each expert are staged in window passes; CMB
+// (down only): the CTA keeps its y rows in shared memory and ends with the
+// slot-ordered combine of its output rows ("DeepSeek-V4-Flash on AMD
+// gfx90a", §8.2 down consumer: FP32 top-k partials and a fixed reduction).
+// Each is a separate instantiation, so the kernel of the other cases keeps
+// its own tight loop.
+template <int MODE, int S, bool WIN, bool CMB = false>
 __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   constexpr int NM = (MODE == kDown) ? 1 : 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -107,6 +116,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   uint8_t *act = reinterpret_cast<uint8_t *>(rowtab + (p.rowtab ? p.cap : 0));
   act = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(act) + 15) & ~uintptr_t(15));
   const uint32_t act_base = smem_addr(act);
+  float *ys = reinterpret_cast<float *>(act + (p.act_smem ? (size_t)p.n_act * p.act_row_bytes : 0));  // [A][R] (CMB)
 
   // Stage the expert offsets in one parallel pass, then list the experts
   // that own rows (ballot compaction keeps increasing id order).
@@ -248,12 +258,35 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
             }
           } else {
             const float v = reduce_one(acc[0]);
-            if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
+            if (lane == 0) {
+              if (CMB) {
+                ys[(int64_t)a * p.R + r] = v;
+                if (p.out0) p.out0[(int64_t)a * p.ld_out + n] = v;
+              } else {
+                p.out0[(int64_t)a * p.ld_out + n] = v;
+              }
+            }
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+    }
+    if constexpr (CMB) {
+      // every expert's y rows of this CTA's output rows are in shared memory:
+      // out[t, n0 + r] = slot-ordered combine, as the stand-alone combine
+      // (fma chain over the slots, a slot of weight exactly 0 adds nothing)
+      bar_sync_named(1, ncons * 32);
+      for (int idx = tid; idx < p.T * p.R; idx += ncons * 32) {
+        const int t = idx / p.R, r = idx - t * p.R;
+        if (r >= R) continue;
+        const float *wt = p.wts + (int64_t)t * p.k;
+        const float *yt = ys + (int64_t)t * p.k * p.R + r;
+        float acc = wt[0] != 0.0f ? __fmul_rn(wt[0], yt[0]) : 0.0f;
+        for (int j = 1; j < p.k; ++j)
+          if (wt[j] != 0.0f) acc = __fmaf_rn(wt[j], yt[(int64_t)j * p.R], acc);
+        p.cout[(int64_t)t * p.ld_cout + n0 + r] = acc;
+      }
     }
     return;
   } else {
@@ -391,13 +424,16 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
     if (budget >= fixed + 2 * (size_t)p.stage_bytes || G >= p.N) break;
     G = (2 * G < p.N) ? 2 * G : p.N;
   }
-  if (budget < fixed + 2 * (size_t)p.stage_bytes)
+  // the fused combine keeps the y rows of this CTA's output rows ([A][R])
+  const bool cmb = MODE == kDown && p.cout != nullptr;
+  const size_t ys_bytes = cmb ? (((size_t)p.A * p.R * 4 + 15) & ~size_t(15)) : 0;
+  if (budget < fixed + ys_bytes + 2 * (size_t)p.stage_bytes)
     return fail(MOE_ERR_UNSUPPORTED, "%s: K=%d too large for the shared-memory ring", name, p.K);
   // every activation row in shared memory if they fit beside a two-stage
   // ring; else, for the light experts of a large batch (the tile policy),
   // two window buffers of up to kWinRows rows each; else rows from global
   // memory (the 1-16-row calls: an expert has one or two rows there)
-  const size_t room = budget - fixed - 2 * (size_t)p.stage_bytes;  // >= 0: checked above
+  const size_t room = budget - fixed - ys_bytes - 2 * (size_t)p.stage_bytes;  // >= 0: checked above
   const size_t all_rows = (size_t)p.n_act * p.act_row_bytes;
   size_t act_bytes = 0;  // never more than room
   p.act_smem = all_rows <= room ? 1 : 0;
@@ -409,21 +445,27 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
     p.win_rows = (int)(w < (size_t)kWinRows ? w : (size_t)kWinRows);
     act_bytes = 2 * (size_t)p.win_rows * p.act_row_bytes;
   }
-  const size_t ns = (budget - fixed - act_bytes) / p.stage_bytes;
+  const size_t ns = (budget - fixed - ys_bytes - act_bytes) / p.stage_bytes;
   p.nstage = ns > 6 ? 6 : (int)ns;
   p.scale16 = (nb % 16) == 0 && (uintptr_t)p.s0 % 16 == 0 && (p.s1 == nullptr || (uintptr_t)p.s1 % 16 == 0);
   const int per_warp = (p.R + 14) / 15;
   const int ncons = (p.R + per_warp - 1) / per_warp;
-  const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + act_bytes;
+  const size_t smem = (size_t)p.nstage * p.stage_bytes + fixed + act_bytes + ys_bytes;
   if (p.nstage < 2 || smem > budget || act_bytes > room)
     return fail(MOE_ERR_UNSUPPORTED, "%s: no shared-memory plan (stages %d, %zu bytes)", name, p.nstage, smem);
   const dim3 block((ncons + 1) * 32);
 
   const bool win = !p.act_smem && p.win_rows > 0;
-  auto kern = win ? (S == 1 ? mx_expert_kernel<MODE, 1, true>
-                            : (S == 2 ? mx_expert_kernel<MODE, 2, true> : mx_expert_kernel<MODE, 4, true>))
-                  : (S == 1 ? mx_expert_kernel<MODE, 1, false>
-                            : (S == 2 ? mx_expert_kernel<MODE, 2, false> : mx_expert_kernel<MODE, 4, false>));
+  if (cmb && win) return fail(MOE_ERR_UNSUPPORTED, "%s: fused combine with activation windows", name);
+  void (*kern)(MxArgs) = win ? (S == 1 ? mx_expert_kernel<MODE, 1, true>
+                                      : (S == 2 ? mx_expert_kernel<MODE, 2, true> : mx_expert_kernel<MODE, 4, true>))
+                             : (S == 1 ? mx_expert_kernel<MODE, 1, false>
+                                      : (S == 2 ? mx_expert_kernel<MODE, 2, false> : mx_expert_kernel<MODE, 4, false>));
+  if constexpr (MODE == kDown) {
+    if (cmb)
+      kern = S == 1 ? mx_expert_kernel<MODE, 1, false, true>
+                    : (S == 2 ? mx_expert_kernel<MODE, 2, false, true> : mx_expert_kernel<MODE, 4, false, true>);
+  }
   const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)budget, name);
   if (ast != MOE_OK) return ast;
   kern<<<G, block, smem, stream>>>(p);
@@ -535,4 +577,42 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
   p.out0 = y; p.ld_out = ld_y;
   p.status = device_status_word();
   return launch_mx<kDown>(p, static_cast<cudaStream_t>(stream), name);
+}
+
+extern "C" moe_status moe_mxfp4_down_combine(const int8_t *hq, int64_t ld_hq, const float *hs, int64_t ld_hs,
+                                             const uint8_t *wd, const uint8_t *sd, const int32_t *offsets,
+                                             const int32_t *sorted, int64_t cap, const float *w, int T, int k, int E,
+                                             int H, int I, float *out, int64_t ld_out, float *y, int64_t ld_y,
+                                             void *stream) {
+  const char *name = "moe_mxfp4_down_combine";
+  moe_status st = check_common(name, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E,
+                               H, I, out, ld_out, I, T * k);
+  if (st != MOE_OK || T == 0) return st;
+  if (!w || (uintptr_t)w % 4) return fail(MOE_ERR_INVALID_ARG, "%s: bad routing weights", name);
+  if (ld_out < H) return fail(MOE_ERR_INVALID_ARG, "%s: ld_out=%lld < H=%d", name, (long long)ld_out, H);
+  if (y && (ld_y < H || (uintptr_t)y % 4)) return fail(MOE_ERR_INVALID_ARG, "%s: bad y output", name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // one launch while the batch keeps the CUDA-core path and a CTA's y rows
+  // fit its shared memory beside the ring
+  const bool split = T >= kTensorMinRows && tc_expert_supported(I, H);
+  if (!split) {
+    MxArgs p{};
+    p.max_rows = 0x7fffffff;
+    p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
+    p.w0 = wd; p.s0 = sd;
+    p.offsets = offsets; p.sorted = sorted; p.cap = cap;
+    p.A = T * k; p.k = k; p.E = E; p.K = I; p.N = H;
+    p.n_act = T * k;
+    p.kdiv = kdiv_of(k);
+    p.out0 = y; p.ld_out = y ? ld_y : 0;
+    p.wts = w; p.cout = out; p.ld_cout = ld_out; p.T = T;
+    p.status = device_status_word();
+    st = launch_mx<kDown>(p, s, name);
+    if (st != MOE_ERR_UNSUPPORTED) return st;
+  }
+  // otherwise the down projection into y, then the combine
+  if (!y) return fail(MOE_ERR_UNSUPPORTED, "%s: T=%d takes two launches and needs the y buffer", name, T);
+  st = moe_mxfp4_down(hq, ld_hq, hs, ld_hs, wd, sd, offsets, sorted, cap, T, k, E, H, I, y, ld_y, stream);
+  if (st != MOE_OK) return st;
+  return moe_combine(y, ld_y, w, T, k, H, out, ld_out, stream);
 }

@@ -15,7 +15,8 @@ import torch
 
 from . import (act_quant_q8, moe_combine, moe_decode_forward, moe_decode_forward_shared, moe_decode_max_tokens,
                moe_decode_max_tokens_shared, moe_decode_workspace_bytes, moe_join_add, moe_mxfp4_down,
-               moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens, moe_sort_tokens_capacity)
+               moe_mxfp4_down_combine, moe_mxfp4_gateup_swiglu, moe_route_topk, moe_sort_tokens,
+               moe_sort_tokens_capacity)
 
 
 @dataclasses.dataclass
@@ -144,7 +145,8 @@ class MoeLayer:
 
         ``events`` optionally maps a stage name ("decode" for the single launch,
         with the shared expert when it fits; "route", "sort", "quant_x",
-        "gateup", "quant_h", "down", "combine" for the stage calls;
+        "gateup", "quant_h", "down", "combine" for the stage calls (below
+        17 rows "down" is the fused down projection and combine);
         "shared_quant_x" (after the single launch only), "shared_gateup",
         "shared_quant_h", "shared_down", "join" for the shared expert's stage
         calls) to a (start, end) pair of torch.cuda.Event recorded around that
@@ -185,8 +187,13 @@ class MoeLayer:
             stage("gateup", moe_mxfp4_gateup_swiglu, ws.xq, ws.xs, lw.wg, lw.sg, lw.wu, lw.su, ws.offsets, ws.sorted,
                   lw.k, ws.h)
             stage("quant_h", act_quant_q8, ws.h, ws.hq, ws.hs)
-            stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
-            stage("combine", moe_combine, ws.y, ws.w, ws.out)
+            if ws.T < 17:
+                # down projection and combine in one launch (y kept as well)
+                stage("down", moe_mxfp4_down_combine, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.w, ws.T,
+                      lw.k, ws.out, ws.y)
+            else:
+                stage("down", moe_mxfp4_down, ws.hq, ws.hs, lw.wd, lw.sd, ws.offsets, ws.sorted, ws.T, lw.k, ws.y)
+                stage("combine", moe_combine, ws.y, ws.w, ws.out)
         if sh is not None:
             # the shared expert: the stage calls on its one-expert weight set
             # (every token, weight 1), then its join onto the routed output
@@ -204,7 +211,7 @@ class MoeLayer:
             if self.lw.shared is None or self.shared_in_one_launch(T):
                 return 1
             return 1 + 5  # the shared expert's quant x, gate/up, quant h, down, join
-        n = 8  # logits, top-k, sort, quant x, gate/up, quant h, down, combine
+        n = 8 if T >= 17 else 7  # logits, top-k, sort, quant x, gate/up, quant h, down (+ combine)
         lw = self.lw
         if T >= 17:  # tile policy: light experts on the CUDA-core kernel, the rest on the tensor-core kernel
             n += (lw.H % 256 == 0 and lw.I % 128 == 0) + (lw.I % 256 == 0 and lw.H % 128 == 0)

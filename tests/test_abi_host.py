@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in _declared():
         assert hasattr(lib, n), n
     assert set(moe.EXPORTS) == _declared()
-    assert lib.moe_abi_version() == 3
+    assert lib.moe_abi_version() == 4
 
 
 def test_library_exports_nothing_else():
@@ -84,6 +84,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.moe_join_add(p, 32, 1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_join_add(p, 64, 1, 64, None, 64, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_join_add(p, 64, -1, 64, p, 64, None) == moe.MOE_ERR_INVALID_ARG
+    # fused down + combine: null routing weights; T = 0 is a no-op
+    assert lib.moe_mxfp4_down_combine(p, 16, p, 1, p, p, p, p, 8, None, 1, 1, 1, 128, 128, p, 128, None, 0,
+                                      None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_mxfp4_down_combine(None, 16, None, 1, None, None, None, None, 0, None, 0, 6, 256, 4096, 2048,
+                                      None, 4096, None, 0, None) == moe.MOE_OK
     # tensor-core probe: unsupported n, iteration count out of range (nothing launched)
     f = C.c_double(0.0)
     assert lib.moe_mxf4_mma_probe(96, 16, C.byref(f), None) == moe.MOE_ERR_INVALID_ARG
