@@ -1,6 +1,7 @@
 // Tensor-core (tcgen05) path of the MXFP4 expert projections, used by the
-// stage calls for batches of more than 16 rows (prefill and large decode
-// batches; the 1-16-row decode regime keeps the CUDA-core kernels).
+// stage calls for the experts with more than 4 rows in batches of more than
+// 16 rows (prefill and large decode batches; the 1-16-row decode regime and
+// the light experts keep the CUDA-core kernels).
 //
 // The layer's projections as grouped GEMMs over the rows routed to each
 // expert: "DeepSeek-V4-Flash on AMD gfx90a", §6.1 (packed FP4 weights with
@@ -156,6 +157,16 @@ MOE_DEVFN void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 MOE_DEVFN void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Bounded mbarrier wait without back-off sleeps, for the short hand-offs of
+// the MMA thread and the drain (try_wait itself suspends the thread for a
+// while); gives up after 2^22 polls.
+MOE_DEVFN bool mbar_wait_spin(uint32_t bar, uint32_t parity, unsigned *status) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  if (status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
+  return false;
+}
 
 // Bounded mbarrier wait taken by a whole warp, with one answer for all lanes.
 MOE_DEVFN bool warp_wait(uint32_t bar, uint32_t parity, unsigned *status) {
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         const bool ext = S.ext[slot][q] != 0;
         for (int s = 0; s < kSteps; ++s) {
           const int j = g * kSteps + s, db = j % ND;
-          ok = warp_wait(smem_addr(&S.d_full[db]), (j / ND) & 1, p.status);
+          ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_addr(&S.d_full[db]), (j / ND) & 1, p.status));
           if (!ok) break;
           tc_fence_after();
           if (active) {
@@ -591,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
         for (int st = 0; st < nstg && ok; ++st) {
           const int g = lt * nstg + st, slot = g % NS;
-          ok = mbar_wait(smem_addr(&S.a_full[slot]), (g / NS) & 1, p.status) &&
-               mbar_wait(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
+          ok = mbar_wait_spin(smem_addr(&S.a_full[slot]), (g / NS) & 1, p.status) &&
+               mbar_wait_spin(smem_addr(&S.b_full[slot]), (g / NS) & 1, p.status);
           if (!ok) break;
           tc_fence_after();
           // descriptors of this stage; the MMAs below only add constant offsets
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
 #pragma unroll
           for (int s = 0; s < kSteps; ++s) {
             const int j = g * kSteps + s, db = j % ND;
-            if (j >= ND && !mbar_wait(smem_addr(&S.d_free[db]), ((j / ND) - 1) & 1, p.status)) {
+            if (j >= ND && !mbar_wait_spin(smem_addr(&S.d_free[db]), ((j / ND) - 1) & 1, p.status)) {
               ok = false;
               break;
             }
