@@ -104,6 +104,10 @@ MOE_DEVFN Misc misc_view(uint8_t *base, int A, int R) {
 }
 
 constexpr uint64_t kBarrierTimeoutNs = 250ull * 1000 * 1000;  // 0.25 s
+// The time limit counts only after this many polls (several milliseconds of
+// polling), so that a step of the global timer (it can be re-synchronised)
+// never ends a wait of normal length.
+constexpr uint32_t kMinPolls = 1u << 14;
 
 MOE_DEVFN uint64_t globaltimer_ns() {
   uint64_t t;
@@ -131,7 +135,7 @@ MOE_DEVFN bool grid_barrier(unsigned long long *ctr, unsigned long long target, 
       unsigned long long v;
       asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if (i > (1u << 26) || globaltimer_ns() - t0 > kBarrierTimeoutNs) {
+      if (i > (1u << 26) || (i > kMinPolls && globaltimer_ns() - t0 > kBarrierTimeoutNs)) {
         ok = 0;
         break;
       }
@@ -152,7 +156,7 @@ MOE_DEVFN bool wait_count(unsigned long long *ctr, unsigned long long target, un
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
     if (v >= target) return true;
-    if (i > (1u << 26) || globaltimer_ns() - t0 > kBarrierTimeoutNs) {
+    if (i > (1u << 26) || (i > kMinPolls && globaltimer_ns() - t0 > kBarrierTimeoutNs)) {
       if (status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
       return false;
     }

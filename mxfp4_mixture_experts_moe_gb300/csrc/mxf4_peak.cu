@@ -31,7 +31,7 @@ MOE_DEVFN bool probe_wait(uint32_t bar, unsigned *status) {
     if (mbar_try_wait(bar, 0)) return true;
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    if (t - t0 > 2000000000ull || i > (1u << 30)) {
+    if ((i > (1u << 14) && t - t0 > 2000000000ull) || i > (1u << 30)) {  // (time counts after 2^14 polls)
       if (status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
       return false;
     }

@@ -210,7 +210,64 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   }
   bar_sync_named(1, ncons * 32);
 
+  // lane 0: the down output of row r for assignment a (CMB: into the CTA's
+  // y rows in shared memory, and to out0 when given)
+  auto put_down = [&](int a, int r, float v) {
+    if (CMB) {
+      ys[(int64_t)a * p.R + r] = v;
+      if (p.out0) p.out0[(int64_t)a * p.ld_out + n0 + r] = v;
+    } else {
+      p.out0[(int64_t)a * p.ld_out + n0 + r] = v;
+    }
+  };
+  // CMB: every expert's y rows of this CTA's output rows are in shared
+  // memory: out[t, n0 + r] = slot-ordered combine, as the stand-alone combine
+  // (fma chain over the slots, a slot of weight exactly 0 adds nothing)
+  auto combine = [&]() {
+    bar_sync_named(1, ncons * 32);
+    for (int idx = tid; idx < p.T * p.R; idx += ncons * 32) {
+      const int t = idx / p.R, r = idx - t * p.R;
+      if (r >= R) continue;
+      const float *wt = p.wts + (int64_t)t * p.k;
+      const float *yt = ys + (int64_t)t * p.k * p.R + r;
+      float acc = wt[0] != 0.0f ? __fmul_rn(wt[0], yt[0]) : 0.0f;
+      for (int j = 1; j < p.k; ++j)
+        if (wt[j] != 0.0f) acc = __fmaf_rn(wt[j], yt[(int64_t)j * p.R], acc);
+      p.cout[(int64_t)t * p.ld_cout + n0 + r] = acc;
+    }
+  };
+
   if constexpr (!WIN) {
+    // assignment and activation row of sorted position q (false: nothing to do)
+    auto resolve = [&](int q, int &a, int &arow) -> bool {
+      if (p.rowtab) {
+        arow = rowtab[q];
+        if (arow < 0) {
+          if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+          return false;
+        }
+        a = p.sorted[q];
+        return true;
+      }
+      a = p.sorted[q];
+      if (a < 0) return false;
+      if (a >= p.A) {
+        if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+        return false;
+      }
+      arow = MODE == kDown ? a : token_of(a, p.kdiv);
+      return true;
+    };
+    // lane 0: the gate/up outputs of row r for assignment a
+    auto put_gateup = [&](int a, int r, float g, float u) {
+      const int64_t o = (int64_t)a * p.ld_out + n0 + r;
+      if (MODE == kGateUpSwiglu) {
+        p.out0[o] = __fmul_rn(silu(g), u);
+      } else {
+        p.out0[o] = g;
+        p.out1[o] = u;
+      }
+    };
     for (int it = 0; it < nact; ++it) {
       const int st = it % nstage;
       if (!mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status)) break;
@@ -218,76 +275,86 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
       const int seg_b = offs[e], seg_e = offs[e + 1];
       const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
 
-      for (int r = warp; r < R; r += ncons) {
-        uint32_t wq[NM][S][8];
-        float ws[NM][S];
-        load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
-        const int n = n0 + r;
+      if constexpr (MODE == kDown) {
+        // more rows than warps: two output rows per warp, u and u + nu, so
+        // that each activation row's loads serve both and one butterfly
+        // reduces both (each row keeps its own arithmetic); not with four
+        // blocks per lane, whose two converted rows would not fit registers
+        const int nu = (S <= 2 && R > ncons) ? (R + 1) >> 1 : 0;
+        for (int r = warp; nu == 0 && r < R; r += ncons) {
+          uint32_t wq[1][S][8];
+          float ws[1][S];
+          load_weights<1, S>(sbase, 0, sbase + p.wreg, 0, r, p.K, wq, ws);
 #pragma unroll 1
-        for (int q = seg_b; q < seg_e; ++q) {
-          int a, arow;
-          if (p.rowtab) {
-            arow = rowtab[q];
-            if (arow < 0) {
-              if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-              continue;
-            }
-            a = p.sorted[q];
-          } else {
-            a = p.sorted[q];
-            if (a < 0) continue;
-            if (a >= p.A) {
-              if (lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-              continue;
-            }
-            arow = MODE == kDown ? a : token_of(a, p.kdiv);
+          for (int q = seg_b; q < seg_e; ++q) {
+            int a, arow;
+            if (!resolve(q, a, arow)) continue;
+            float acc[1];
+            if (p.act_smem) row_dot_smem<1, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+            else row_dot_global<1, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+            const float v = reduce_one(acc[0]);
+            if (lane == 0) put_down(a, r, v);
           }
-          float acc[NM];
-          if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
-          else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
-          if (NM == 2) {
+        }
+        for (int u = warp; u < nu; u += ncons) {
+          const int r2 = u + nu < R ? u + nu : u;
+          const uint32_t dw = (uint32_t)(r2 - u) * (p.K / 2), dsc = (uint32_t)(r2 - u) * nb;
+          uint32_t wq[2][S][8];
+          float ws[2][S];
+          load_weights<2, S>(sbase, dw, sbase + p.wreg, dsc, u, p.K, wq, ws);
+#pragma unroll 1
+          for (int q = seg_b; q < seg_e; ++q) {
+            int a, arow;
+            if (!resolve(q, a, arow)) continue;
+            float acc[2];
+            if (p.act_smem) row_dot_smem<2, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+            else row_dot_global<2, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
+            float v0, v1;
+            reduce_pair(acc[0], acc[1], v0, v1);
+            if (lane == 0) {
+              put_down(a, u, v0);
+              if (r2 != u) put_down(a, r2, v1);
+            }
+          }
+        }
+      } else if (p.act_smem && seg_e - seg_b == 1) {
+        // an expert with one row: the weights are read from the stage and
+        // decoded by sign for that row alone (fewer integer operations than
+        // converting them once for several rows); the same block dots
+        int a, arow;
+        if (resolve(seg_b, a, arow)) {
+          for (int r = warp; r < R; r += ncons) {
+            const uint32_t wrow[2] = {sbase + (uint32_t)r * (p.K / 2), sbase + p.wreg + (uint32_t)r * (p.K / 2)};
+            const uint32_t srow[2] = {sbase + 2 * p.wreg + (uint32_t)r * nb, sbase + 2 * p.wreg + p.sreg + (uint32_t)r * nb};
+            float acc[2];
+            row_dot_stage_pn<2, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wrow, srow, acc);
+            float g, u;
+            reduce_pair(acc[0], acc[1], g, u);
+            if (lane == 0) put_gateup(a, r, g, u);
+          }
+        }
+      } else {
+        for (int r = warp; r < R; r += ncons) {
+          uint32_t wq[NM][S][8];
+          float ws[NM][S];
+          load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
+#pragma unroll 1
+          for (int q = seg_b; q < seg_e; ++q) {
+            int a, arow;
+            if (!resolve(q, a, arow)) continue;
+            float acc[NM];
+            if (p.act_smem) row_dot_smem<NM, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wq, ws, acc);
+            else row_dot_global<NM, S>(p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, p.K, wq, ws, acc);
             float g, u;
             reduce_pair(acc[0], acc[NM - 1], g, u);
-            if (lane == 0) {
-              if (MODE == kGateUpSwiglu) {
-                p.out0[(int64_t)a * p.ld_out + n] = __fmul_rn(silu(g), u);
-              } else {
-                p.out0[(int64_t)a * p.ld_out + n] = g;
-                p.out1[(int64_t)a * p.ld_out + n] = u;
-              }
-            }
-          } else {
-            const float v = reduce_one(acc[0]);
-            if (lane == 0) {
-              if (CMB) {
-                ys[(int64_t)a * p.R + r] = v;
-                if (p.out0) p.out0[(int64_t)a * p.ld_out + n] = v;
-              } else {
-                p.out0[(int64_t)a * p.ld_out + n] = v;
-              }
-            }
+            if (lane == 0) put_gateup(a, r, g, u);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
     }
-    if constexpr (CMB) {
-      // every expert's y rows of this CTA's output rows are in shared memory:
-      // out[t, n0 + r] = slot-ordered combine, as the stand-alone combine
-      // (fma chain over the slots, a slot of weight exactly 0 adds nothing)
-      bar_sync_named(1, ncons * 32);
-      for (int idx = tid; idx < p.T * p.R; idx += ncons * 32) {
-        const int t = idx / p.R, r = idx - t * p.R;
-        if (r >= R) continue;
-        const float *wt = p.wts + (int64_t)t * p.k;
-        const float *yt = ys + (int64_t)t * p.k * p.R + r;
-        float acc = wt[0] != 0.0f ? __fmul_rn(wt[0], yt[0]) : 0.0f;
-        for (int j = 1; j < p.k; ++j)
-          if (wt[j] != 0.0f) acc = __fmaf_rn(wt[j], yt[(int64_t)j * p.R], acc);
-        p.cout[(int64_t)t * p.ld_cout + n0 + r] = acc;
-      }
-    }
+    if constexpr (CMB) combine();
     return;
   } else {
   // activation row of sorted position q (-1: padding, -2: out of range)
@@ -359,7 +426,36 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
       pbuf ^= 1;
       if (pit < nact) copy_pass(pit, pc0, pbuf);  // the next pass's rows, while this one is computed
       if (dead) continue;
-      for (int r = warp; r < R; r += ncons) {
+      // the down projection: two output rows per warp when there are more
+      // rows than warps (as in the loop above)
+      const int nu = (MODE == kDown && S <= 2 && R > ncons) ? (R + 1) >> 1 : 0;
+      if constexpr (MODE == kDown) {
+        for (int u = warp; u < nu; u += ncons) {
+          const int r2 = u + nu < R ? u + nu : u;
+          uint32_t wq[2][S][8];
+          float ws[2][S];
+          load_weights<2, S>(sbase, (uint32_t)(r2 - u) * (p.K / 2), sbase + p.wreg, (uint32_t)(r2 - u) * nb, u, p.K,
+                             wq, ws);
+#pragma unroll 1
+          for (int q = c0; q < c1; ++q) {
+            const int arow = row_of(q);
+            if (arow < 0) {
+              if (arow == -2 && lane == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
+              continue;
+            }
+            const int a = p.sorted[q];
+            float acc[2];
+            row_dot_smem<2, S>(wrows + (uint32_t)(q - c0) * p.act_row_bytes, p.K, wq, ws, acc);
+            float v0, v1;
+            reduce_pair(acc[0], acc[1], v0, v1);
+            if (lane == 0) {
+              put_down(a, u, v0);
+              if (r2 != u) put_down(a, r2, v1);
+            }
+          }
+        }
+      }
+      for (int r = warp; nu == 0 && r < R; r += ncons) {
         uint32_t wq[NM][S][8];
         float ws[NM][S];
         load_weights<NM, S>(sbase, p.wreg, sbase + NM * p.wreg, p.sreg, r, p.K, wq, ws);
@@ -387,7 +483,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
             }
           } else {
             const float v = reduce_one(acc[0]);
-            if (lane == 0) p.out0[(int64_t)a * p.ld_out + n] = v;
+            if (lane == 0) put_down(a, r, v);
           }
         }
       }
@@ -432,7 +528,8 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   // every activation row in shared memory if they fit beside a two-stage
   // ring; else, for the light experts of a large batch (the tile policy),
   // two window buffers of up to kWinRows rows each; else rows from global
-  // memory (the 1-16-row calls: an expert has one or two rows there)
+  // memory (the 1-16-row calls: an expert has one or two rows there, and a
+  // barrier per window pass costs more than the L2 reads it saves)
   const size_t room = budget - fixed - ys_bytes - 2 * (size_t)p.stage_bytes;  // >= 0: checked above
   const size_t all_rows = (size_t)p.n_act * p.act_row_bytes;
   size_t act_bytes = 0;  // never more than room

@@ -109,6 +109,100 @@ route_logits_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, i
   }
 }
 
+// Small batches (T <= kSmallMaxT): one CTA per kSmallE experts x kSmallT
+// tokens takes its whole router rows and token rows in one round of bulk
+// copies (no slab pipeline: at a few tokens the slabs' serial round trips
+// were the whole cost), then warp w dots expert w / 2 against four tokens
+// at once.  Same per-logit order as route_logits_kernel.
+constexpr int kSmallE = 2, kSmallT = 8, kSmallWarps = 4, kSmallMaxT = 16;
+
+MOE_DEVFN uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+template <bool XBF, bool WBF>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+route_logits_small_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits,
+                          unsigned *status) {
+  extern __shared__ __align__(128) uint8_t rsm[];
+  __shared__ __align__(8) uint64_t bar;
+  constexpr uint32_t xsz = XBF ? 2 : 4, wsz = WBF ? 2 : 4;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e0 = blockIdx.x * kSmallE, t0 = blockIdx.y * kSmallT;
+  const int ne = min(kSmallE, E - e0), nt = min(kSmallT, T - t0);
+  const uint32_t wrow_bytes = (uint32_t)H * wsz, xrow_bytes = (uint32_t)H * xsz;
+  const uint32_t wbase = smem_addr(rsm), xbase = wbase + kSmallE * wrow_bytes;
+  const uint32_t fb = smem_addr(&bar);
+  if (tid == 0) {
+    mbar_init(fb, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(fb, (uint32_t)ne * wrow_bytes + (uint32_t)nt * xrow_bytes);
+    const uint64_t wpol = policy_evict_first(), xpol = policy_evict_last();  // x is read by every CTA
+    for (int i = 0; i < ne; ++i)
+      bulk_g2s(wbase + (uint32_t)i * wrow_bytes, static_cast<const uint8_t *>(wr) + (int64_t)(e0 + i) * wrow_bytes,
+               wrow_bytes, fb, wpol);
+    for (int j = 0; j < nt; ++j)
+      bulk_g2s(xbase + (uint32_t)j * xrow_bytes, static_cast<const uint8_t *>(x) + (int64_t)(t0 + j) * ld_x * xsz,
+               xrow_bytes, fb, xpol);
+  }
+  if (!mbar_wait(fb, 0, status)) {
+    mbar_wait(fb, 0, nullptr);  // once more (bounded) before leaving with copies in flight
+    return;
+  }
+  const int el = warp >> 1, tl0 = 4 * (warp & 1);
+  if (el >= ne || tl0 >= nt) return;
+  const int nj = min(4, nt - tl0);
+  const uint32_t wrow = wbase + (uint32_t)el * wrow_bytes, xrow = xbase + (uint32_t)tl0 * xrow_bytes;
+  float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const int nch = H / 8;
+#pragma unroll 1
+  for (int c = lane; c < nch; c += 32) {
+    float wv[8];
+    load8_smem(wrow + (uint32_t)c * 8 * wsz, WBF, wv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < nj) {
+        float xv[8];
+        load8_smem(xrow + (uint32_t)j * xrow_bytes + (uint32_t)c * 8 * xsz, XBF, xv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) p[j] = __fmaf_rn(xv[q], wv[q], p[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], s));
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (lane == j && j < nj) logits[(int64_t)(t0 + tl0 + j) * E + e0 + el] = p[j];
+}
+
+// The small-batch kernel when T and its shared memory allow (else false).
+bool launch_route_logits_small(bool xbf, bool wbf, const void *x, int64_t ld_x, const void *wr, int T, int H, int E,
+                               float *logits, cudaStream_t s, cudaError_t *err) {
+  if (T > kSmallMaxT) return false;
+  const size_t smem = (size_t)kSmallE * H * (wbf ? 2 : 4) + (size_t)kSmallT * H * (xbf ? 2 : 4);
+  if (smem > 200 * 1024) return false;
+  void (*kern)(const void *, int64_t, const void *, int, int, int, float *, unsigned *) =
+      xbf ? (wbf ? route_logits_small_kernel<true, true> : route_logits_small_kernel<true, false>)
+          : (wbf ? route_logits_small_kernel<false, true> : route_logits_small_kernel<false, false>);
+  if (smem > 48 * 1024 &&
+      ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)smem, "moe_route_topk") != MOE_OK) {
+    *err = cudaErrorInvalidValue;
+    return true;
+  }
+  const dim3 grid((E + kSmallE - 1) / kSmallE, (T + kSmallT - 1) / kSmallT);
+  kern<<<grid, kSmallWarps * 32, smem, s>>>(x, ld_x, wr, T, H, E, logits, device_status_word());
+  *err = cudaGetLastError();
+  return true;
+}
+
 template <int EW, bool XBF, bool WBF>
 cudaError_t launch_route_logits(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits,
                                 cudaStream_t s) {
@@ -176,9 +270,11 @@ extern "C" moe_status moe_route_topk(const void *x, moe_dtype x_dtype, int64_t l
   if ((T + kRouteTokens - 1) / kRouteTokens > 65535) return fail(MOE_ERR_UNSUPPORTED, "moe_route_topk: T=%d too large", T);
   // experts per warp: more CTAs for small batches, more reuse of each staged input for large ones
   const bool xbf = x_dtype == MOE_BF16, wbf = w_dtype == MOE_BF16;
-  cudaError_t err = T <= 8    ? launch_route_logits_dt<1>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
-                    : T <= 64 ? launch_route_logits_dt<2>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
-                              : launch_route_logits_dt<4>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s);
+  cudaError_t err = cudaSuccess;
+  if (!launch_route_logits_small(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s, &err))
+    err = T <= 8    ? launch_route_logits_dt<1>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
+          : T <= 64 ? launch_route_logits_dt<2>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s)
+                    : launch_route_logits_dt<4>(xbf, wbf, x, ld_x, w_router, T, H, E, logits, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_route_topk: logits launch");
   topk_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, bias, T, E, k, ids, weights);
   err = cudaGetLastError();
