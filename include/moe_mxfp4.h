@@ -31,6 +31,12 @@
  * Conventions shared by every call
  *  - All pointers are DEVICE pointers owned by the caller; the library never
  *    allocates, frees or retains them, and never synchronises the stream.
+ *    Its own scratch: the tensor-core path of the expert projections (calls
+ *    of 17 rows or more) writes the activations' E2M1 planes to a buffer it
+ *    allocates and frees on the call's stream (stream-ordered, from a memory
+ *    pool of the library's that keeps its memory between calls; about
+ *    6 * (K / 2) + 6 * K / 32 + 4 bytes per sorted position); the single-
+ *    launch decode calls need the workspace they are given and nothing else.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *    enqueue work; results are ready when the stream reaches them.
  *  - Matrices are row-major; ld_* are row strides in ELEMENTS of that array.
@@ -48,10 +54,11 @@
  *    one-row call, so a T-row call gives, row by row, the bits of T one-row
  *    calls (stage calls and the single-launch decode path alike).  Routing,
  *    the sorter, Q8 and the combine keep that for every T.  From 17 rows on,
- *    the expert projections of experts with many rows run on the tensor
- *    cores, which form the same exact block terms but add them in increasing
- *    block order: those rows agree with the one-row call within fp32
- *    rounding (the layer's tolerance), not bit for bit.
+ *    the expert projections of experts with more than 4 rows run on the
+ *    tensor cores, which take each activation value as six E2M1 planes with
+ *    their own E8M0 scales (about 1e-5 of the output's RMS, exact for unit
+ *    scales) and accumulate the whole reduction in fp32: those rows agree
+ *    with the one-row call within the layer's tolerance, not bit for bit.
  *  - Requires an sm_103a device (GB300); MOE_ERR_UNSUPPORTED otherwise.
  *
  * Weight layout (one layer; E experts; all contiguous, 16-byte aligned):

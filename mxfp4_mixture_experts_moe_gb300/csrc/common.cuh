@@ -158,24 +158,44 @@ MOE_DEVFN void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One poll of an mbarrier phase.  The thread may be suspended inside the
+// poll until the phase completes; the hint caps that at 20 us, so that the
+// bounds below are bounds in time.
 MOE_DEVFN bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^22 polls (well over a second with the
-// back-off), raises MOE_DEV_WAIT_TIMEOUT and returns false.
+MOE_DEVFN uint64_t gtimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Limits of a bounded mbarrier wait: two seconds of global time, counted
+// only once kWaitMinPolls polls have passed (so that a step of the global
+// timer, which can be re-synchronised, never ends a wait of normal length),
+// or kWaitMaxPolls polls.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitMinPolls = 1u << 12;
+constexpr uint32_t kWaitMaxPolls = 1u << 24;
+
+// Bounded wait: gives up at the limits above, raises MOE_DEV_WAIT_TIMEOUT
+// and returns false.
 MOE_DEVFN bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status) {
-  for (uint32_t i = 0; i < (1u << 22); ++i) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < kWaitMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i >= 16) __nanosleep(64);
+    if (i == 64) t0 = gtimer_ns();
+    else if (i > kWaitMinPolls && (i & 255u) == 0 && gtimer_ns() - t0 > kWaitLimitNs) break;
   }
   if (status) atomicOr(status, MOE_DEV_WAIT_TIMEOUT);
   return false;
@@ -195,6 +215,11 @@ MOE_DEVFN void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t 
 MOE_DEVFN uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+MOE_DEVFN uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

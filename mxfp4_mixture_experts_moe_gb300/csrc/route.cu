@@ -116,12 +116,6 @@ route_logits_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, i
 // at once.  Same per-logit order as route_logits_kernel.
 constexpr int kSmallE = 2, kSmallT = 8, kSmallWarps = 4, kSmallMaxT = 16;
 
-MOE_DEVFN uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 template <bool XBF, bool WBF>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 route_logits_small_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits,

@@ -54,6 +54,13 @@ MOE_DEVFN uint32_t idesc_mxf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The descriptor with the scale-factor IDs of A and B set: the byte of the
+// 32-bit tensor-memory word at which the MMA's scales start (0 or 2 with
+// two scales per row, scale_vec::2X), bits 29-30 for A and 4-5 for B.
+MOE_DEVFN uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (a_id << 29) | (b_id << 4);
+}
+
 // D[tmem] (+)= A * B with per-32 block scales from tensor memory (sfa, sfb).
 MOE_DEVFN void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                         bool accumulate) {

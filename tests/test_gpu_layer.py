@@ -89,10 +89,11 @@ def _check_vs_oracle(spec, x, lw_ws, out, sample=None):
     hq_g = host(ws.hq)[arows].astype(np.int32)
     hq_o = r["hq"].astype(np.int32)
     hs_o = r["hs"].astype(np.float32)
-    # a scale is amax/127 of its block of h, so it carries h's relative error:
-    # ~1e-7 on the CUDA-core path, ~1e-5 where the tensor core accumulates the
-    # 4096-term reductions in its own fp32 order (batches beyond 16 rows)
-    assert np.allclose(host(ws.hs)[arows], hs_o, rtol=1e-4, atol=0)
+    # a scale is amax/127 of its block of h, so it carries h's error: ~1e-7
+    # of the scale on the CUDA-core path; on the tensor path (batches beyond
+    # 16 rows, activations as E2M1 planes) h is held to the layer's tolerance,
+    # max|err| <= TOL * RMS(h) <= TOL * amax, and so is the scale
+    assert np.allclose(host(ws.hs)[arows], hs_o, rtol=TOL, atol=0)
     flip = hq_g != hq_o
     assert np.all(np.abs(hq_g - hq_o) <= 1)
     # y then differs by at most |dq| * scale * max|w| (|w| <= 6 for E8M0 <= 127)

@@ -49,7 +49,9 @@ def _check_shared_output(ws, r):
     hq_g = host(ws.sh_hq).astype(np.int32)
     hq_o = r["hq"].astype(np.int32)
     hs_o = r["hs"].astype(np.float64)
-    assert np.allclose(host(ws.sh_hs), hs_o, rtol=1e-4, atol=0)
+    # the scales carry h's error: fp32 rounding up to 16 rows; beyond, the
+    # tensor path's h is held to the layer's tolerance (max|err| <= TOL * RMS)
+    assert np.allclose(host(ws.sh_hs), hs_o, rtol=TOL, atol=0)
     flip = hq_g != hq_o
     assert np.all(np.abs(hq_g - hq_o) <= 1)
     allow = (np.repeat(hs_o, 32, axis=1) * flip * 6.0).sum(axis=1)  # |w| <= 6 (E8M0 <= 127)

@@ -182,8 +182,12 @@ def test_gateup(moe, H, I, E, k, T, exact):
         assert bits_equal(host(g), Go.astype(np.float32))
         assert bits_equal(host(u), Uo.astype(np.float32))
     else:
-        assert max_err_over_rms(host(g), Go) <= 1e-5
-        assert max_err_over_rms(host(u), Uo) <= 1e-5
+        # fp32 rounding alone on the CUDA-core path (up to 16 rows); from 17
+        # rows the tensor path, whose six E2M1 planes of the activations leave
+        # ~1e-5 (bound 1e-4, inside the layer's 1e-3)
+        bound = 1e-5 if T < 17 else 1e-4
+        assert max_err_over_rms(host(g), Go) <= bound
+        assert max_err_over_rms(host(u), Uo) <= bound
     # SwiGLU output: h = silu(G) * U
     h = torch.full((T * k, I + 8), float("nan"), device="cuda")[:, :I]
     moe.moe_mxfp4_gateup_swiglu(dev(xq), dev(xs), W["wg"], W["sg"], W["wu"], W["su"], dev(offsets), dev(srt), k, h)

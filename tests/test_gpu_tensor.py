@@ -1,17 +1,17 @@
 """The tensor-core (tcgen05) expert projections, taken by the stage calls for
 batches of more than 16 rows, against the oracle.
 
-The tensor path keeps the layer's exact block dots: E2M1 weights with their
-E8M0 byte as the MMA block scale, the Q8 codes as three base-8 digit
-planes, one fp32 accumulator per block (exact), then acc = fma(D, xs, acc)
-block by block.  With unit scales every block term is an integer and every output is
-exact, so those cases are compared bit for bit with the oracle; with the
-layer's scales the order of the fp32 accumulation differs from the oracle's,
-so the bar is the layer's tolerance, max|err| <= 1e-3 * RMS.  Cases span
-several 128-row weight tiles, experts with more than 32 rows (several token
-tiles), experts with a handful of rows, padded segments, and reduction
-lengths from 256 to 4096 (the tensor path needs a multiple of 256; other
-shapes keep the CUDA-core path).
+The tensor path gives the MMA the E2M1 weights with their E8M0 byte as the
+block scale, and each activation value q * xs as six E2M1 planes with E8M0
+block scales of their own (a greedy expansion, about two bits per plane);
+the accumulator takes the whole reduction in fp32.  With unit scales (xs =
+1, E8M0 bytes 128) the planes hold every Q8 code exactly and every output is
+a sum of integer block dots, so those cases are compared bit for bit with
+the oracle; with the layer's scales the bar is the layer's tolerance,
+max|err| <= 1e-3 * RMS.  Cases span several 128-row weight tiles, experts
+with more than 16 rows (several token tiles), experts with a handful of
+rows, padded segments, and reduction lengths from 256 to 4096 (the tensor
+path needs a multiple of 256; other shapes keep the CUDA-core path).
 """
 import numpy as np
 import pytest
