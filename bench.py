@@ -73,6 +73,9 @@ KERNEL_SOURCES = {
     "moe_mxfp4_gateup_swiglu": ["tc_expert.cu", "tc_device.cuh", "mxmv.cu", "mx_device.cuh", "common.cuh"],
 }
 ARITHMETIC = "e2m1*int8 exact int32 block dots, fp32 scale and accumulate"
+# batches of 17+ rows: experts of more than 4 rows on the tensor cores
+ARITHMETIC_TENSOR = ("e2m1*int8 exact int32 block dots (experts of <= 4 rows); e2m1 weights x six e2m1 planes "
+                     "of the Q8 activations, fp32 MMA accumulation (more rows)")
 
 
 def source_hash(kernel: str) -> str:
@@ -652,7 +655,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": ARITHMETIC, "data": "synthetic",
+            "vs_baseline": None, "dtype": ARITHMETIC if T < 17 else ARITHMETIC_TENSOR, "data": "synthetic",
             "config": workload_config(args.workload, world, args.shared_expert),
             "run": {"l2": f"{NL} layer copies x {r['NX']} token batches cycled ({NL * 3.42:.1f} GB of weights > L2)",
                     "graph": f"CUDA graphs of {r['S']} consecutive layer forwards (distinct layer copies), "
