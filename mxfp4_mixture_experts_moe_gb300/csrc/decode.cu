@@ -21,6 +21,7 @@
 // Waits are bounded: a grid barrier or an mbarrier that does not complete in
 // about a second sets MOE_DEV_WAIT_TIMEOUT and the kernel returns.
 #include <algorithm>
+#include <atomic>
 
 #include "mx_device.cuh"
 
@@ -108,6 +109,12 @@ constexpr uint64_t kBarrierTimeoutNs = 250ull * 1000 * 1000;  // 0.25 s
 // polling), so that a step of the global timer (it can be re-synchronised)
 // never ends a wait of normal length.
 constexpr uint32_t kMinPolls = 1u << 14;
+
+// Programmatic dependent launch: wait until the kernels this launch depends
+// on have completed and their writes are visible (returns at once when the
+// launch was not programmatic); allow the kernel after this one to launch.
+MOE_DEVFN void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEVFN void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 MOE_DEVFN uint64_t globaltimer_ns() {
   uint64_t t;
@@ -423,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   const int n0g = (int)((unsigned)(cta * I) / (unsigned)G), Rg = (int)((unsigned)((cta + 1) * I) / (unsigned)G) - n0g;
   const int n0d = (int)((unsigned)(cta * H) / (unsigned)G), Rd = (int)((unsigned)((cta + 1) * H) / (unsigned)G) - n0d;
 
+  // the next kernel on the stream may be launched now; its CTAs start on SMs
+  // as this launch's CTAs leave them, and wait for this launch to complete
+  // before they touch anything it uses (programmatic dependent launch)
+  grid_dependents_launch();
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bars);
   uint64_t *empty = full + nstage;
   const uint32_t act = smem_addr(smem + p.off_act);
@@ -458,6 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         bulk_g2s(front + (uint32_t)w * H * wsz, static_cast<const uint8_t *>(p.wr) + (int64_t)e * H * wsz, H * wsz,
                  smem_addr(fbar), pol);
     }
+  }
+  // Everything above reads only this launch's weights.  From here on the
+  // kernel reads x and the workspace and writes its outputs, which the kernel
+  // before it on the stream may still be using when this one was launched
+  // early (programmatic dependent launch): wait for that kernel to complete.
+  grid_dependency_wait();
+  if (tid == 0) {
+    const uint64_t pol = policy_evict_first();
     for (int t = 0; t < T; ++t)
       bulk_g2s(xs_smem + (uint32_t)t * H * xsz, static_cast<const uint8_t *>(p.x) + (int64_t)t * p.ld_x * xsz, H * xsz,
                smem_addr(fbar), pol);
@@ -1103,12 +1122,25 @@ moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, in
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  // cooperative (every CTA resident: the grid barrier) and programmatic
+  // (this launch may begin while the kernel before it finishes; it waits for
+  // it before reading x or the workspace).  Without programmatic launches the
+  // kernel runs unchanged: its wait then returns at once.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  static std::atomic<int> pdl{1};  // cleared if the runtime refuses the pair
+  cfg.numAttrs = pdl.load() ? 2 : 1;
   err = cudaLaunchKernelEx(&cfg, kern, p);
+  if (err != cudaSuccess && cfg.numAttrs == 2) {
+    (void)cudaGetLastError();
+    pdl.store(0);
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, p);
+  }
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, name);
 }
 
