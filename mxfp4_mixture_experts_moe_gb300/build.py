@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "cuda")
 LIB = os.path.join(PKG, "libmoe_mxfp4.so")
 SOURCES = ["abi.cu", "route.cu", "sort.cu", "quant.cu", "mxmv.cu", "combine.cu", "decode.cu", "decode_noalloc.cu",
-           "tc_expert.cu", "mxf4_peak.cu"]
+           "tc_expert.cu", "mxf4_peak.cu", "krow.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

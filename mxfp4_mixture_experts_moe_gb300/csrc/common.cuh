@@ -43,6 +43,17 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
                             int K, int N, int bytoken, int min_rows, float *out0, float *out1, int64_t ld_out,
                             cudaStream_t stream, const char *name);
 
+// The expert projections of 1-16-row calls (krow.cu): mode 0 gate/up with
+// SwiGLU into out0, 1 gate into out0 and up into out1, 2 down into out0 (and
+// the slot-ordered combine into cout when cout is given), over the experts
+// with at most max_rows rows.  MOE_ERR_UNSUPPORTED (nothing enqueued) when the
+// shape does not fit its shared-memory plan.
+moe_status launch_krow(int mode, const int8_t *aq, int64_t ld_aq, const float *as, int64_t ld_as, const uint8_t *w0,
+                       const uint8_t *s0, const uint8_t *w1, const uint8_t *s1, const int32_t *offsets,
+                       const int32_t *sorted, int64_t cap, int T, int k, int E, int K, int N, int max_rows,
+                       float *out0, float *out1, int64_t ld_out, const float *wts, float *cout, int64_t ld_cout,
+                       cudaStream_t stream, const char *name);
+
 // The single-launch decode forward (decode.cu) behind moe_decode_forward and
 // moe_decode_forward_shared: their arguments, the shared expert's (sh, or
 // null), and clear_ws: zero the workspace on the stream right before the

@@ -663,6 +663,13 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
                           0, kLightExpertRows, y, nullptr, ld_y, static_cast<cudaStream_t>(stream), name);
     if (st != MOE_OK) return st;
   }
+  if (!split) {
+    // 1-16 rows: the four-group kernel (krow.cu) when its shared-memory plan
+    // fits the shape; the kernel below otherwise
+    st = launch_krow(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E, I, H,
+                     0x7fffffff, y, nullptr, ld_y, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream), name);
+    if (st != MOE_ERR_UNSUPPORTED) return st;
+  }
   MxArgs p{};
   p.max_rows = split ? kLightExpertRows : 0x7fffffff;
   p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
@@ -693,6 +700,9 @@ extern "C" moe_status moe_mxfp4_down_combine(const int8_t *hq, int64_t ld_hq, co
   // fit its shared memory beside the ring
   const bool split = T >= kTensorMinRows && tc_expert_supported(I, H);
   if (!split) {
+    st = launch_krow(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E, I, H,
+                     0x7fffffff, y, nullptr, y ? ld_y : 0, w, out, ld_out, s, name);
+    if (st != MOE_ERR_UNSUPPORTED) return st;
     MxArgs p{};
     p.max_rows = 0x7fffffff;
     p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
