@@ -663,13 +663,13 @@ extern "C" moe_status moe_mxfp4_down(const int8_t *hq, int64_t ld_hq, const floa
                           0, kLightExpertRows, y, nullptr, ld_y, static_cast<cudaStream_t>(stream), name);
     if (st != MOE_OK) return st;
   }
-  if (!split) {
-    // 1-16 rows: the four-group kernel (krow.cu) when its shared-memory plan
-    // fits the shape; the kernel below otherwise
-    st = launch_krow(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E, I, H,
-                     0x7fffffff, y, nullptr, ld_y, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream), name);
-    if (st != MOE_ERR_UNSUPPORTED) return st;
-  }
+  // the four-group kernel (krow.cu) for every expert of a 1-16-row call, or
+  // the light experts of a larger one, when its shared-memory plan fits the
+  // shape; the kernel below otherwise
+  st = launch_krow(2, hq, ld_hq, hs, ld_hs, wd, sd, nullptr, nullptr, offsets, sorted, cap, T, k, E, I, H,
+                   split ? kLightExpertRows : 0x7fffffff, y, nullptr, ld_y, nullptr, nullptr, 0,
+                   static_cast<cudaStream_t>(stream), name);
+  if (st != MOE_ERR_UNSUPPORTED) return st;
   MxArgs p{};
   p.max_rows = split ? kLightExpertRows : 0x7fffffff;
   p.aq = hq; p.ld_aq = ld_hq; p.as = hs; p.ld_as = ld_hs;
