@@ -31,6 +31,7 @@ constexpr int kKrowThreads = 32 * (kConsWarps + 1);  // + the producer warp
 constexpr int kKrowMaxStages = 8;
 constexpr int kKrowMaxAct = 4;  // activation rows staged with an item, at most
 
+
 enum KrowMode { kKGateUp = 0, kKGateUpRaw = 1, kKDown = 2 };
 
 struct KrowArgs {

@@ -618,6 +618,14 @@ static moe_status gateup_impl(int mode, const int8_t *xq, int64_t ld_xq, const f
                           name);
     if (st != MOE_OK) return st;
   }
+  if (split) {
+    // the light experts of a 17+-row call: the four-group kernel (krow.cu)
+    // when its plan fits (for 1-16-row calls the kernel below is faster: it
+    // converts the weights of an expert with several rows once)
+    st = launch_krow(mode == kGateUpSwiglu ? 0 : 1, xq, ld_xq, xs, ld_xs, wg, sg, wu, su, offsets, sorted, cap, T, k,
+                     E, H, I, kLightExpertRows, o0, o1, ld, nullptr, nullptr, 0, s, name);
+    if (st != MOE_ERR_UNSUPPORTED) return st;
+  }
   MxArgs p{};
   p.max_rows = split ? kLightExpertRows : 0x7fffffff;
   p.aq = xq; p.ld_aq = ld_xq; p.as = xs; p.ld_as = ld_xs;
