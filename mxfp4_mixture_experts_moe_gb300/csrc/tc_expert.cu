@@ -65,13 +65,11 @@ namespace moe {
 namespace {
 
 constexpr int kRows = 128;                       // weight rows per tile (MMA M)
-constexpr int kNT = 16;                          // activation rows per tile, at most
+constexpr int kNTMax = 32;                       // activation rows per tile, at most (NT = 16 or 32)
 constexpr int kPlanes = 6;                       // E2M1 planes per activation row
-constexpr int kN = kPlanes * kNT;                // MMA N: plane p's rows at [16 p, 16 p + 16)
 constexpr int kStageK = 256;                     // reduction elements per stage (8 MX blocks)
 constexpr int kSteps = kStageK / 64;             // MMA K-steps per stage
 constexpr uint32_t kAMat = kRows * kStageK / 2;  // one matrix's packed weights per stage (16 KB)
-constexpr uint32_t kBStage = kN * kStageK / 2;   // the planes of a stage (12 KB)
 constexpr int kDrainWarps = 8;
 constexpr int kPrepWarps = 4;
 constexpr int kWarpTma = kDrainWarps + kPrepWarps;
@@ -127,9 +125,9 @@ struct TcShared {
   int mrow[2];         // first output row of the tile within its expert
   int64_t wrow[2];     // first weight row of the tile (expert * N + mrow)
   int col0[2];         // first sorted position of the tile
-  int colrow[2][kNT];  // activation row of each column (row 0 for a column without one)
-  int colasg[2][kNT];  // output row (assignment) of each column (-1: none)
-  int colext[2][kNT];  // the column's activation row takes the exact fallback
+  int colrow[2][kNTMax];  // activation row of each column (row 0 for a column without one)
+  int colasg[2][kNTMax];  // output row (assignment) of each column (-1: none)
+  int colext[2][kNTMax];  // the column's activation row takes the exact fallback
   int ext[2][4];       // per table buffer and quadrant: a weight byte outside the clamp range
   int prefix[1];       // [E + 1] tiles before expert e
 };
@@ -323,6 +321,7 @@ struct Tile {
   int col0;  // first sorted position of the tile
 };
 
+template <int NT>
 MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   // expert: last e with prefix[e] <= t (binary search over E+1 entries)
   int lo = 0, hi = p.E;
@@ -337,8 +336,8 @@ MOE_DEVFN Tile tile_of(const TcShared &S, const TcArgs &p, int t, int mt) {
   tl.mtile = local % mt;
   const int ntile = local / mt;
   const int b = p.offsets[lo], n_e = p.offsets[lo + 1] - b;
-  tl.col0 = b + ntile * kNT;
-  tl.ncols = min(kNT, n_e - ntile * kNT);
+  tl.col0 = b + ntile * NT;
+  tl.ncols = min(NT, n_e - ntile * NT);
   return tl;
 }
 
@@ -358,12 +357,18 @@ MOE_DEVFN int column_assignment(const TcArgs &p, const Tile &tl, int c, bool fla
 }
 MOE_DEVFN int column_row(const TcArgs &p, int a) { return a < 0 ? 0 : (p.bytoken ? token_of(a, p.kdiv) : a); }
 
-template <int MODE>
+template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, const __grid_constant__ TcMaps maps) {
   constexpr int NM = MODE == kDownMode ? 1 : 2;
-  // per slot: A scales (4 columns per matrix and K-step pair), B scales (4 per pair)
-  constexpr uint32_t kSlotCols = 4u * (kSteps / 2) * (NM + 1);
-  constexpr uint32_t kDBase = kTmemCols - 2u * NM * kN;   // two accumulator buffers
+  constexpr int kN = kPlanes * NT;                      // MMA N: plane p's rows at [NT p, NT p + NT)
+  constexpr uint32_t kBStage = kN * kStageK / 2;        // the planes of a stage
+  constexpr int ND = (NM == 2 && NT == 32) ? 1 : 2;     // accumulator buffers
+  constexpr int kSfbGroups = kN / 32;                   // 32-row groups of B (its scale columns)
+  // per slot: A scales (4 columns per matrix and K-step pair), B scales (4
+  // or 8 per pair: one per 32-row group of B)
+  constexpr uint32_t kSfbCols = (kSfbGroups + 3) & ~3;
+  constexpr uint32_t kSlotCols = 4u * (kSteps / 2) * NM + kSfbCols * (kSteps / 2);
+  constexpr uint32_t kDBase = kTmemCols - (uint32_t)(ND * NM * kN);
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
   const uint32_t dyn = smem_addr(smem_dyn);
   const uint32_t pad = ((dyn + 1023u) & ~1023u) - dyn;
@@ -377,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
   const uint32_t s_a = sb + p.off_a, s_b = sb + p.off_b;
   // K-step s's scales: bytes 2 (s & 1), + 1 of the pair's column
   auto sfa_col = [&](int slot, int s, int m) { return (uint32_t)slot * kSlotCols + 4u * (uint32_t)((s >> 1) * NM + m); };
-  auto sfb_col = [&](int slot, int s) { return (uint32_t)slot * kSlotCols + 4u * (kSteps / 2) * NM + 4u * (uint32_t)(s >> 1); };
+  auto sfb_col = [&](int slot, int s) {
+    return (uint32_t)slot * kSlotCols + 4u * (kSteps / 2) * NM + kSfbCols * (uint32_t)(s >> 1);
+  };
   auto d_col = [&](int buf, int m) { return kDBase + (uint32_t)(buf * NM + m) * kN; };
 
   if (tid == 0) {
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
         const int b = p.offsets[e], en = p.offsets[e + 1];
         const bool bad = b < 0 || en < b || en > p.cap;
         if (bad && p.status) atomicOr(p.status, MOE_DEV_BAD_ROW);
-        if (!bad && en - b > p.min_rows) nt = ((en - b + kNT - 1) / kNT) * mt;
+        if (!bad && en - b > p.min_rows) nt = ((en - b + NT - 1) / NT) * mt;
       }
       int incl = nt;
 #pragma unroll
@@ -428,47 +435,54 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
 
   if (warp < kDrainWarps) {
     // ------------------------------------------------ epilogue
+    constexpr int kHalf = NT / 2;  // activation rows (columns) per epilogue warp
     const int q = warp & 3, h = warp >> 2;
     const uint32_t lanes = (uint32_t)(32 * q) << 16;
     const int r = 32 * q + lane;  // weight row of the tile = tensor-memory lane
     bool ok = true;
     for (int lt = 0; lt < my_tiles && ok; ++lt) {
       const int tb = lt & 1, ph = (lt >> 1) & 1;
+      const int buf = lt % ND, bph = (lt / ND) & 1;
       ok = warp_wait(smem_addr(&S.tab_full[tb]), ph, p.status) &&
-           __all_sync(0xffffffffu, mbar_wait_spin(smem_addr(&S.d_full[tb]), ph, p.status));
+           __all_sync(0xffffffffu, mbar_wait_spin(smem_addr(&S.d_full[buf]), bph, p.status));
       if (!ok) break;
       tc_fence_after();
       const int ncols = S.ncols[tb];
-      float v[NM][8];
-      if (8 * h < ncols) {
+      const int c0 = kHalf * h;  // this warp's first column
+      float v[NM][kHalf];
+      if (c0 < ncols) {
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
-          uint32_t d[kPlanes][8];
 #pragma unroll
-          for (int pl = 0; pl < kPlanes; ++pl) tmem_ld8_nowait(tmem + lanes + d_col(tb, m) + 16u * pl + 8u * h, d[pl]);
-          tmem_ld_wait();
-          // the planes' partial sums, smallest first
+          for (int c8 = 0; c8 < kHalf; c8 += 8) {
+            uint32_t d[kPlanes][8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float s = __uint_as_float(d[kPlanes - 1][j]);
+            for (int pl = 0; pl < kPlanes; ++pl)
+              tmem_ld8_nowait(tmem + lanes + d_col(buf, m) + (uint32_t)(NT * pl + c0 + c8), d[pl]);
+            tmem_ld_wait();
+            // the planes' partial sums, smallest first
 #pragma unroll
-            for (int pl = kPlanes - 2; pl >= 0; --pl) s = __fadd_rn(s, __uint_as_float(d[pl][j]));
-            v[m][j] = s;
+            for (int j = 0; j < 8; ++j) {
+              float s = __uint_as_float(d[kPlanes - 1][j]);
+#pragma unroll
+              for (int pl = kPlanes - 2; pl >= 0; --pl) s = __fadd_rn(s, __uint_as_float(d[pl][j]));
+              v[m][c8 + j] = s;
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.d_free[tb]));
+      if (lane == 0) mbar_arrive(smem_addr(&S.d_free[buf]));
       // the tile's weight-byte flags (complete once every stage was prepared)
       ok = warp_wait(smem_addr(&S.ext_full[tb]), ph, p.status);
       if (!ok) break;
-      if (8 * h < ncols) {
+      if (c0 < ncols) {
         const bool exta = S.ext[tb][q] != 0;
         const int64_t orow = (int64_t)S.mrow[tb] + r;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = 8 * h + j;
+        for (int j = 0; j < kHalf; ++j) {
+          const int c = c0 + j;
           const int a = c < ncols ? S.colasg[tb][c] : -1;
           if (a < 0) continue;
           float o[NM];
@@ -502,43 +516,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
       ok = warp_wait(smem_addr(&S.tab_full[tb]), (lt >> 1) & 1, p.status);
       if (!ok) break;
       const int64_t wrow = S.wrow[tb] + 32 * q + lane;  // this lane's weight row (A scales)
-      // operand rows n = 32 c + lane of B (plane n / 16, column n % 16): their
+      // operand rows n = 32 c + lane of B (plane n / NT, column n % NT): their
       // scale bytes, in column group c of every quadrant
-      const uint8_t *brow[3];
+      const uint8_t *brow[kSfbGroups];
 #pragma unroll
-      for (int c = 0; c < 3; ++c) {
+      for (int c = 0; c < kSfbGroups; ++c) {
         const int n = 32 * c + lane;
-        brow[c] = p.bsc + ((int64_t)min(S.col0[tb] + n % kNT, p.npos - 1) * kPlanes + n / kNT) * nbk;
+        brow[c] = p.bsc + ((int64_t)min(S.col0[tb] + n % NT, p.npos - 1) * kPlanes + n / NT) * nbk;
       }
       uint32_t outside = 0;
       // the scale bytes of a stage are requested kAhead stages before they
       // are stored, so their load latency overlaps the stages between
-      constexpr int kAhead = 3;
-      uint2 ra[kAhead][NM], rb[kAhead][3];
-      auto load_scales = [&](int st, uint2 (&a)[NM], uint2 (&b)[3]) {
+      constexpr int kAhead = NT == 16 ? 3 : 2;
+      uint2 ra[kAhead][NM], rb[kAhead][kSfbGroups];
+      auto load_scales = [&](int st, uint2 (&a)[NM], uint2 (&b)[kSfbGroups]) {
         if (st < nstg) {
 #pragma unroll
           for (int m = 0; m < NM; ++m)
             a[m] = __ldg(reinterpret_cast<const uint2 *>((m == 0 ? p.s0 : p.s1) + wrow * nbk + st * 8));
 #pragma unroll
-          for (int c = 0; c < 3; ++c) b[c] = __ldg(reinterpret_cast<const uint2 *>(brow[c] + st * 8));
+          for (int c = 0; c < kSfbGroups; ++c) b[c] = __ldg(reinterpret_cast<const uint2 *>(brow[c] + st * 8));
         }
       };
 #pragma unroll
       for (int i = 0; i < kAhead; ++i) load_scales(i, ra[i], rb[i]);
       for (int st = 0; st < nstg && ok; ++st) {
         const int g = lt * nstg + st, slot = g % NS;
-        uint2 sfw[NM], bfw[3];
+        uint2 sfw[NM], bfw[kSfbGroups];
 #pragma unroll
         for (int m = 0; m < NM; ++m) sfw[m] = ra[0][m];
 #pragma unroll
-        for (int c = 0; c < 3; ++c) bfw[c] = rb[0][c];
+        for (int c = 0; c < kSfbGroups; ++c) bfw[c] = rb[0][c];
 #pragma unroll
         for (int i = 0; i + 1 < kAhead; ++i) {
 #pragma unroll
           for (int m = 0; m < NM; ++m) ra[i][m] = ra[i + 1][m];
 #pragma unroll
-          for (int c = 0; c < 3; ++c) rb[i][c] = rb[i + 1][c];
+          for (int c = 0; c < kSfbGroups; ++c) rb[i][c] = rb[i + 1][c];
         }
         load_scales(st + kAhead, ra[kAhead - 1], rb[kAhead - 1]);
         if (g >= NS) {
@@ -554,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
           tmem_st1(tmem + lanes + sfa_col(slot, 2, m) + (uint32_t)q, clamp_e8m0x4(sfw[m].y));
         }
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
+        for (int c = 0; c < kSfbGroups; ++c) {
           tmem_st1(tmem + lanes + sfb_col(slot, 0) + (uint32_t)c, bfw[c].x);
           tmem_st1(tmem + lanes + sfb_col(slot, 2) + (uint32_t)c, bfw[c].y);
         }
@@ -579,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
       const uint64_t pol = policy_evict_first(), keep = policy_evict_last();
       bool ok = true;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const Tile tl = tile_of(S, p, cta + lt * G, mt);
+        const Tile tl = tile_of<NT>(S, p, cta + lt * G, mt);
         const int row0 = tl.e * p.N + tl.mtile * kRows;
         for (int st = 0; st < nstg; ++st) {
           const int g = lt * nstg + st, slot = g % NS;
@@ -595,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
           // the tile's 16 sorted positions of each plane: operand rows 16 pl ..
 #pragma unroll
           for (int pl = 0; pl < kPlanes; ++pl)
-            tma_load_2d(s_b + (uint32_t)slot * kBStage + (uint32_t)pl * (kNT * kStageK / 2), &maps.b,
+            tma_load_2d(s_b + (uint32_t)slot * kBStage + (uint32_t)pl * (NT * kStageK / 2), &maps.b,
                         st * (kStageK / 2), pl * p.npos + tl.col0, bar, keep);
         }
       }
@@ -608,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
       const uint64_t adesc0 = smem_desc_sw128(s_a), bdesc0 = smem_desc_sw128(s_b);
       bool ok = true;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const int buf = lt & 1;
-        if (lt >= 2 && !mbar_wait_spin(smem_addr(&S.d_free[buf]), ((lt >> 1) - 1) & 1, p.status)) break;
+        const int buf = lt % ND;
+        if (lt >= ND && !mbar_wait_spin(smem_addr(&S.d_free[buf]), ((lt / ND) - 1) & 1, p.status)) break;
         tc_fence_after();
         for (int st = 0; st < nstg && ok; ++st) {
           const int g = lt * nstg + st, slot = g % NS;
@@ -638,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(const TcArgs p, 
   } else {
     // ------------------------------------------------ column tables, one tile ahead
     for (int lt = 0; lt < my_tiles; ++lt) {
-      const Tile tl = tile_of(S, p, cta + lt * G, mt);
+      const Tile tl = tile_of<NT>(S, p, cta + lt * G, mt);
       const int tb = lt & 1;
       if (lt >= 2 && !warp_wait(smem_addr(&S.tab_empty[tb]), ((lt >> 1) - 1) & 1, p.status)) break;
-      if (lane < kNT) {
+      if (lane < NT) {
         const int a = column_assignment(p, tl, lane, true);
         const int row = column_row(p, a);
         S.colasg[tb][lane] = a;
@@ -695,13 +709,13 @@ bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t col
 }
 
 // The activation planes [rows][cols bytes] as a 2-D tensor map with boxes of
-// 128 bytes x 16 rows (one plane's rows of a tile), 128-byte swizzled.
-bool encode_planes(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols) {
+// 128 bytes x nt rows (one plane's rows of a tile), 128-byte swizzled.
+bool encode_planes(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, int nt) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {128u, (cuuint32_t)kNT};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)nt};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -770,12 +784,19 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
     if (!encode_rows(&maps.w[m], m == 0 ? w0 : w1, wrows, (uint64_t)K / 2))
       return fail(MOE_ERR_UNSUPPORTED, "%s: tensor maps of the weights could not be built (16-byte aligned weights are required)", name);
   }
+  // token tiles of 32 rows when the experts average many rows (fewer weight
+  // reads from shared memory per row; gate/up then has one accumulator
+  // buffer), else of 16 rows
+  const int nt = (int64_t)A >= 48ll * E ? 32 : 16;
+  const int kn = kPlanes * nt;
+  const int nd = (nm == 2 && nt == 32) ? 1 : 2;
+  const uint32_t bstage = (uint32_t)kn * kStageK / 2;
   // tensor memory: per stage slot 4 columns per matrix and K-step pair (A
-  // scales) and 4 per pair (B scales); the two accumulator buffers at the top
-  const uint32_t slot_cols = 4u * (kSteps / 2) * (uint32_t)(nm + 1);
-  const int ns_tmem = (int)((kTmemCols - 2u * (uint32_t)nm * kN) / slot_cols);
+  // scales) and 4 or 8 per pair (B scales); the accumulator buffers at the top
+  const uint32_t slot_cols = 4u * (kSteps / 2) * (uint32_t)nm + ((uint32_t)(kn / 32 + 3) & ~3u) * (kSteps / 2);
+  const int ns_tmem = (int)((kTmemCols - (uint32_t)(nd * nm * kn)) / slot_cols);
   // shared memory: the stage ring (packed weights, planes), then the small state
-  const uint32_t stage = (uint32_t)nm * kAMat + kBStage;
+  const uint32_t stage = (uint32_t)nm * kAMat + bstage;
   const size_t fixed = (size_t)tc_shared_bytes(E) + 1024u + 64u;
   int ns = (int)(((size_t)optin - fixed) / stage);
   if (ns > kMaxStages) ns = kMaxStages;
@@ -784,10 +805,13 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
   p.nstage = ns;
   p.off_a = 0;  // 1024-aligned (swizzled copies)
   p.off_b = (uint32_t)ns * nm * kAMat;
-  p.off_misc = (p.off_b + (uint32_t)ns * kBStage + 63u) & ~63u;
+  p.off_misc = (p.off_b + (uint32_t)ns * bstage + 63u) & ~63u;
   const size_t smem = (size_t)p.off_misc + tc_shared_bytes(E) + 1024u;  // + alignment of the base
   if (smem > (size_t)optin) return fail(MOE_ERR_UNSUPPORTED, "%s: tensor path needs %zu bytes of shared memory", name, smem);
-  auto kern = mode == kSwiglu ? tc_expert_kernel<kSwiglu> : mode == kRaw ? tc_expert_kernel<kRaw> : tc_expert_kernel<kDownMode>;
+  auto kern = nt == 32 ? (mode == kSwiglu ? tc_expert_kernel<kSwiglu, 32>
+                                           : mode == kRaw ? tc_expert_kernel<kRaw, 32> : tc_expert_kernel<kDownMode, 32>)
+                       : (mode == kSwiglu ? tc_expert_kernel<kSwiglu, 16>
+                                          : mode == kRaw ? tc_expert_kernel<kRaw, 16> : tc_expert_kernel<kDownMode, 16>);
   const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), optin, name);
   if (ast != MOE_OK) return ast;
 
@@ -803,7 +827,7 @@ moe_status launch_tc_expert(int mode, const int8_t *aq, int64_t ld_aq, const flo
   uint8_t *planes = static_cast<uint8_t *>(buf);
   p.bsc = planes + plane_bytes;
   p.bflag = reinterpret_cast<const int *>(planes + plane_bytes + bsc_bytes);
-  if (!encode_planes(&maps.b, planes, (uint64_t)kPlanes * npos, (uint64_t)K / 2)) {
+  if (!encode_planes(&maps.b, planes, (uint64_t)kPlanes * npos, (uint64_t)K / 2, nt)) {
     cudaFreeAsync(buf, stream);
     return fail(MOE_ERR_UNSUPPORTED, "%s: tensor map of the activation planes could not be built", name);
   }
