@@ -387,6 +387,38 @@ MOE_DEVFN void ring_slot(int it, int nslot, int NS, bool hqr, int &st, int &use)
   use = (nslot - st + NS - 1) / NS + d / NSd;  // gate/up items on stage st, then earlier down items
 }
 
+// Full barrier (index into the kernel's full barriers) and phase parity of
+// ring item it.  The routed gate/up items alternate between the two consumer
+// groups, and each group waits only on barriers of its own, one per (stage,
+// group) at 2 st + g, in order.  The items every consumer warp waits for
+// (the shared expert's gate/up item, then the down items) have a third
+// barrier per stage, at 2 NS + st.  With one barrier per stage for both
+// groups, an odd number of stages would let a group reach its item's phase
+// while the other group's item before it on that stage has not landed, and
+// a parity wait cannot tell those phases apart.
+MOE_DEVFN void ring_full(int it, int s0, int nslot, int NS, bool hqr, int &bar, uint32_t &parity) {
+  int st, use;
+  ring_slot(it, nslot, NS, hqr, st, use);
+  if (it >= s0 && it < nslot) {
+    const int j = it - s0, L = (NS & 1) ? 2 * NS : NS;  // items (stage, group) repeat every lcm(NS, 2)
+    bar = 2 * st + (j & 1);
+    parity = (uint32_t)(j / L) & 1u;
+  } else {
+    int n = 0;  // earlier all-warp items on stage st
+    if (it >= nslot) {
+      const int d = it - nslot;
+      n = (hqr ? d / (NS - 1) : d / NS) + ((s0 && st == 0) ? 1 : 0);
+    }
+    bar = 2 * NS + st;
+    parity = (uint32_t)n & 1u;
+  }
+}
+// The barrier of ring item it on stage st (ring_full's index without its
+// divisions; the hot loops track the phase parities themselves).
+MOE_DEVFN int ring_full_bar(int it, int st, int s0, int nslot, int NS) {
+  return (it >= s0 && it < nslot) ? 2 * st + ((it - s0) & 1) : 2 * NS + st;
+}
+
 // The producer warp's copies of one gate/up slice (rows row0 .. of both
 // matrices, Rg rows each) into the ring stage at sbase, completing on the
 // stage's full barrier fb (the whole warp calls it: the scale bytes may need
@@ -435,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // before they touch anything it uses (programmatic dependent launch)
   grid_dependents_launch();
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bars);
-  uint64_t *empty = full + nstage;
+  uint64_t *empty = full + 3 * nstage;  // full: 2 per stage (one per consumer group), then 1 per stage for all warps
   const uint32_t act = smem_addr(smem + p.off_act);
   float *yslice = reinterpret_cast<float *>(smem + p.off_y);
   float *logit_s = reinterpret_cast<float *>(smem + p.off_logit);
@@ -448,12 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   constexpr int s0 = SHARED ? 1 : 0;  // gate/up ring items before the routed slots (the shared expert's)
   const uint32_t front = smem_addr(smem) + (s0 ? p.stage_bytes : 0u);
   const uint32_t xs_smem = front + (uint32_t)nrw * H * wsz;
-  uint64_t *fbar = full + 2 * nstage;
+  uint64_t *fbar = full + 4 * nstage;
   if (tid == 0) {
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
-      mbar_init(smem_addr(&empty[s]), kGroup);
-    }
+    for (int s = 0; s < 3 * nstage; ++s) mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx + 32 cp.async arrives
+    for (int s = 0; s < nstage; ++s) mbar_init(smem_addr(&empty[s]), kGroup);
     mbar_init(smem_addr(fbar), 1);
     fence_mbar_init();
     m.scalars[4] = 0;
@@ -495,13 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // requested at once, into stage 0
   if constexpr (SHARED) {
     if (warp == kCons)
-      gateup_copies(smem_addr(smem), smem_addr(&full[0]), p.swg, p.swu, p.ssg, p.ssu, n0g, (uint32_t)Rg * (H / 2),
+      gateup_copies(smem_addr(smem), smem_addr(&full[2 * nstage]), p.swg, p.swu, p.ssg, p.ssu, n0g, (uint32_t)Rg * (H / 2),
                     (uint32_t)Rg * nbH, p, H, nbH, policy_evict_first());
   }
   // a CTA that gives up before the ring runs first lets that copy land
   // (bounded), so no copy is still writing its shared memory when it exits
   auto settle_shared = [&]() {
-    if (s0 && warp == kCons) mbar_wait(smem_addr(&full[0]), 0, p.status);
+    if (s0 && warp == kCons) mbar_wait(smem_addr(&full[2 * nstage]), 0, p.status);
   };
   if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(fbar), 0, p.status))) {
     settle_shared();
@@ -557,9 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // producer warp calls it: the scale bytes may need per-lane copies)
   const uint64_t pol = policy_evict_first();
   const uint32_t gwb = (uint32_t)Rg * (H / 2), gsb = (uint32_t)Rg * nbH;
-  auto issue_gateup = [&](int st, int expert) {
-    gateup_copies(smem_addr(smem + (size_t)st * p.stage_bytes), smem_addr(&full[st]), p.wg, p.wu, p.sg, p.su,
-                  (int64_t)expert * I + n0g, gwb, gsb, p, H, nbH, pol);
+  auto issue_gateup = [&](int it, int expert) {
+    const int st = it % nstage;
+    gateup_copies(smem_addr(smem + (size_t)st * p.stage_bytes), smem_addr(&full[2 * st + ((it - s0) & 1)]), p.wg, p.wu,
+                  p.sg, p.su, (int64_t)expert * I + n0g, gwb, gsb, p, H, nbH, pol);
   };
   int early = s0;  // gate/up ring items the producer already requested
   if (T == 1) {
@@ -667,9 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       ring_slot(it, nslot, nstage, p.hqr, st, use);
       if (use >= 1 && !mbar_wait(smem_addr(&empty[st]), (use - 1) & 1, p.status)) break;
       const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
-      const uint32_t fb = smem_addr(&full[st]);
+      const uint32_t fb = smem_addr(&full[ring_full_bar(it, st, s0, nslot, nstage)]);
       if (it < nslot) {
-        issue_gateup(st, m.active[it - s0]);  // it >= early >= s0: the shared item went out at the start
+        issue_gateup(it, m.active[it - s0]);  // it >= early >= s0: the shared item went out at the start
       } else {
         const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
         if (lane == 0) {
@@ -698,18 +729,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       if (it == first - 1) prefetch_down();
     }
     // before exiting, the latest copy into every stage has landed: the last
-    // item issued into each stage (1 + its use count, 16 bits per stage; with
-    // hqr the down items skip the last stage, so its latest copy can be a
-    // gate/up item long before the end)
+    // item issued into each stage (1 + its index, 16 bits per stage; with hqr
+    // the down items skip the last stage, so its latest copy can be a gate/up
+    // item long before the end)
     uint64_t last = 0;
     for (int it = 0; it < issued; ++it) {
       int st, use;
       ring_slot(it, nslot, nstage, p.hqr, st, use);
-      last = (last & ~(0xFFFFull << (16 * st))) | ((uint64_t)(use + 1) << (16 * st));
+      last = (last & ~(0xFFFFull << (16 * st))) | ((uint64_t)(it + 1) << (16 * st));
     }
     for (int st = 0; st < nstage; ++st) {
-      const int u1 = (int)((last >> (16 * st)) & 0xFFFFu);
-      if (u1) mbar_wait(smem_addr(&full[st]), (u1 - 1) & 1, p.status);
+      const int i1 = (int)((last >> (16 * st)) & 0xFFFFu);
+      if (i1) {
+        int fbi;
+        uint32_t par;
+        ring_full(i1 - 1, s0, nslot, nstage, p.hqr, fbi, par);
+        mbar_wait(smem_addr(&full[fbi]), par, p.status);
+      }
     }
     return;
   }
@@ -743,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       for (int t = lane; t < T; t += 32) m.srt[nq0 + t] = A + t;
       if (lane == 0) m.segb[nact + 1] = nq0 + T;
     }
-    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[0]), 0, p.status));
+    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[2 * nstage]), 0, p.status));
     if (!dead) {
       const uint32_t sbase = smem_addr(smem);
 #pragma unroll 1
@@ -764,10 +800,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar + kSharedWord), "l"(1ull) : "memory");
     if (grp == 0 && lane == 0) mbar_arrive(smem_addr(&empty[0]));
   }
-  for (int it = s0 + grp; it < nslot; it += 2) {
-    const int st = it % nstage;
+  // this group's next phase parity on its barrier of each stage (bit st)
+  uint32_t gpar = 0;
+  for (int it = s0 + grp, st = (s0 + grp) % nstage; it < nslot;
+       it += 2, st = st + 2 >= nstage ? st + 2 - nstage : st + 2) {  // st: stage of item it
     const int js = it - s0;  // routed slot
-    if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / nstage) & 1, p.status));
+    if (!dead)
+      dead = !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[2 * st + grp]), (gpar >> st) & 1u, p.status));
+    gpar ^= 1u << st;
     const uint32_t sbase = smem_addr(smem + (size_t)st * p.stage_bytes);
     if (!dead) {
       const int sb = m.segb[js], se = m.segb[js + 1];
@@ -847,10 +887,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   // the activation loads), then group 0 releases the stage.  Slice j < nact
   // is routed slot j; slice nact the shared expert (its y rows follow the
   // A routed ones in the slice buffer)
+  uint32_t apar = s0 ? 1u : 0u;  // next phase parity of the all-warp barrier of each stage (bit st)
   for (int it = nslot; it < nslot + ndi; ++it) {
     int st, use;
     ring_slot(it, nslot, nstage, p.hqr, st, use);
-    if (!broken && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), use & 1, p.status))) broken = dead = true;
+    if (!broken && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[2 * nstage + st]), (apar >> st) & 1u, p.status)))
+      broken = dead = true;
+    apar ^= 1u << st;
     if (!dead) {
       const int j0 = (it - nslot) * p.dpp, j1 = min(nslot, j0 + p.dpp);
       for (int j = j0 + grp; j < j1; j += 2) {
@@ -970,7 +1013,7 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
   const uint64_t cand_bytes = (uint64_t)T * 8 * 8 * 8;  // top-k candidates: T x 8 groups x 8 (key, id)
   const uint64_t misc_bytes = align16(4ull * (5 * A + rows + 2 + 8));  // ids w srt skey segb active + 8 scalars
-  const uint64_t small = 16ull * 8 + y_bytes + logit_bytes + cand_bytes + misc_bytes;
+  const uint64_t small = 32ull * 8 + y_bytes + logit_bytes + cand_bytes + misc_bytes;
   const uint64_t budget = (uint64_t)optin - 1024;
   auto stages = [&](uint64_t tail) { return tail >= budget ? 0 : std::min<int>(4, (int)((budget - tail) / p.stage_bytes)); };
   // Q8(h) in the region of Q8(x) (both outside the ring), or in the last
@@ -988,7 +1031,7 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
                                           (p.shared ? p.stage_bytes : 0) + align16(front));
   if (ring + tail > budget) return false;
   p.off_bars = (uint32_t)ring;
-  p.off_act = p.off_bars + 16 * 8;
+  p.off_act = p.off_bars + 32 * 8;  // 4 NS + 1 <= 17 mbarriers; the activation rows stay 128-byte aligned
   p.off_hq = p.off_act;
   p.off_y = p.off_act + (uint32_t)(p.hqr ? act_bytes : std::max(act_bytes, hq_bytes));
   p.off_logit = p.off_y + (uint32_t)y_bytes;

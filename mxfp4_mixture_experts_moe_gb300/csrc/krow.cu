@@ -129,18 +129,23 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
   const int NS = p.nstage;
 
   uint8_t *stages = smem;
+  // A full barrier per (stage, group): the groups take every kGroups-th item
+  // and the stages cycle with another period, so on one stage-wide barrier a
+  // group could come to its phase while an earlier item of another group on
+  // that stage has not landed, which a parity wait cannot tell apart.  Each
+  // group waits on its own barriers in order; item it arms barrier
+  // (it % NS, it % kGroups), phase it / lcm(NS, kGroups).
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NS * p.stage_bytes);
-  uint64_t *empty = full + NS;
+  uint64_t *empty = full + NS * kGroups;
+  const int L = NS % kGroups == 0 ? NS : NS % 2 == 0 ? 2 * NS : kGroups * NS;  // lcm(NS, kGroups = 4)
   int *active = reinterpret_cast<int *>(empty + NS);  // [E]
   int *offs = active + p.E;                           // [E+1]
   float *ys = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(offs + p.E + 1) + 15) & ~uintptr_t(15));  // [A][R] (CMB)
 
   for (int i = tid; i <= p.E; i += blockDim.x) offs[i] = p.offsets[i];
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
-      mbar_init(smem_addr(&empty[s]), kGroupWarps);
-    }
+    for (int s = 0; s < NS * kGroups; ++s) mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx + 32 cp.async arrives
+    for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&empty[s]), kGroupWarps);
     fence_mbar_init();
   }
   __syncthreads();
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
       const uint32_t wbytes = (uint32_t)(r1 - r0) * (K / 2), sbytes = (uint32_t)(r1 - r0) * nb;
       const int64_t row0 = (int64_t)e * p.N + n0 + r0;
       const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
-      const uint32_t fb = smem_addr(&full[st]);
+      const uint32_t fb = smem_addr(&full[st * kGroups + it % kGroups]);
       const int seg_b = offs[e], nq = min(offs[e + 1] - seg_b, p.armax);
       // the staged activation rows: positions seg_b .. seg_b + nq - 1 (slot j
       // = position seg_b + j; a position without a valid assignment is skipped)
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
     }
     // never leave with copies in flight into this CTA's shared memory
     for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
-      mbar_wait(smem_addr(&full[it % NS]), (it / NS) & 1, p.status);
+      mbar_wait(smem_addr(&full[(it % NS) * kGroups + it % kGroups]), (it / L) & 1, p.status);
     return;
   }
 
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
   };
   for (int it = grp; it < nitem; it += kGroups) {
     const int st = it % NS;
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st]), (it / NS) & 1, p.status))) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[st * kGroups + grp]), (it / L) & 1, p.status))) break;
     const int e = active[it / NH];
     int r0, r1;
     item_rows(it, r0, r1);
@@ -377,7 +382,7 @@ moe_status launch_krow(int mode, const int8_t *aq, int64_t ld_aq, const float *a
   p.s16 = (nb % 16) == 0 && (uintptr_t)s0 % 16 == 0 && (s1 == nullptr || (uintptr_t)s1 % 16 == 0);
   p.as16 = (uintptr_t)as % 16 == 0 && ld_as % 4 == 0;
   const bool cmb = mode == kKDown && cout != nullptr;
-  const size_t fixed = 2 * 8 * kKrowMaxStages + 4 * (size_t)(2 * E + 1) + 16 +
+  const size_t fixed = (kGroups + 1) * 8 * kKrowMaxStages + 4 * (size_t)(2 * E + 1) + 16 +
                        (cmb ? (size_t)p.A * p.R * 4 + 16 : 0) + 64;
   const size_t budget = (size_t)optin - 1024;
   if (budget < fixed) return fail(MOE_ERR_UNSUPPORTED, "%s: no shared-memory plan", name);

@@ -25,7 +25,7 @@ constexpr int kRouteSlab = 64;   // 8-element chunks per shared-memory slab (512
 template <int EW, bool XBF, bool WBF>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_logits_kernel(const void *x, int64_t ld_x, const void *wr, int T, int H, int E, float *logits) {
-  extern __shared__ __align__(16) uint8_t rsm[];
+  extern __shared__ __align__(128) uint8_t rsm[];
   constexpr uint32_t xsz = XBF ? 2 : 4, wsz = WBF ? 2 : 4;
   constexpr uint32_t wrow = kRouteSlab * 8 * wsz, xrow = kRouteSlab * 8 * xsz;  // bytes per row and slab
   constexpr int nw = kRouteWarps * EW;                                            // router rows per tile

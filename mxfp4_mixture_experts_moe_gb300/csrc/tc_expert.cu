@@ -169,14 +169,6 @@ MOE_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, u
       : "memory");
 }
 
-
-// Byte offset of 16-byte chunk j of row r in a K-major operand of 128-byte
-// rows, 128-byte swizzled (8-row groups of 1024 bytes, chunk index XOR row
-// within the group): the layout the TMA writes for the weights.
-MOE_DEVFN uint32_t sw128_ofs(int r, int j) {
-  return (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u + (uint32_t)((j ^ (r & 7)) * 16);
-}
-
 // Eight floats rounded to E2M1 (round to nearest, ties to even, saturating
 // at +-6), element i in nibble i of the result (the weights' packing).
 MOE_DEVFN uint32_t e2m1x8_from_f32(const float (&t)[8]) {
