@@ -472,6 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
   float *yslice = reinterpret_cast<float *>(smem + p.off_y);
   float *logit_s = reinterpret_cast<float *>(smem + p.off_logit);
   const Misc m = misc_view(smem + p.off_misc, A, A + (SHARED ? T : 0));
+  // the scale-factor table (not for H = 2048 full-shape builds, where its
+  // extra loads spill registers)
+  constexpr bool kTab = !(FULL && SG == 2);
+  __shared__ __align__(16) uint32_t e8m0_tab[256];  // static: its address is a constant, not a register
+  const uint32_t stab = smem_addr(e8m0_tab);
+  fill_e8m0_table(stab);  // published by the first barrier below
 
   const int nrw = (E + G - 1) / G;  // router warps in this kernel (host ensures <= 8)
   const uint32_t wsz = p.wbf ? 2u : 4u, xsz = p.xbf ? 2u : 4u;
@@ -789,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
         const uint32_t srow[2] = {sbase + 2 * p.gwreg + (uint32_t)r * nbH,
                                   sbase + 2 * p.gwreg + p.gsreg + (uint32_t)r * nbH};
         float acc[2];
-        row_dot_stage_pn<2, SG>(act + (uint32_t)t * p.xrow, H, wrow, srow, acc);
+        row_dot_stage_pn<2, SG, kTab>(act + (uint32_t)t * p.xrow, H, wrow, srow, stab, acc);
         float g, u2;
         reduce_pair(acc[0], acc[1], g, u2);
         if (lane == 0) p.sh_h[(int64_t)t * p.ld_sh_h + n0g + r] = __fmul_rn(silu(g), u2);
@@ -821,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
           const int a = m.srt[q];
           const int t = token_of(a, p.kdiv);
           float acc[2];
-          row_dot_stage_pn<2, SG>(act + (uint32_t)t * p.xrow, H, wrow, srow, acc);
+          row_dot_stage_pn<2, SG, kTab>(act + (uint32_t)t * p.xrow, H, wrow, srow, stab, acc);
           float g, u;
           reduce_pair(acc[0], acc[1], g, u);
           if (lane == 0) p.h[(int64_t)a * p.ld_h + n0g + r] = __fmul_rn(silu(g), u);
@@ -909,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs p)
           for (int q = sb; q < se; ++q) {
             const int a = m.srt[q];
             float acc[2];
-            row_dot_stage_pn<2, SD>(hq + (uint32_t)q * p.hrow, I, wrow, srow, acc);
+            row_dot_stage_pn<2, SD, kTab>(hq + (uint32_t)q * p.hrow, I, wrow, srow, stab, acc);
             float v0, v1;
             reduce_pair(acc[0], acc[1], v0, v1);
             if (lane == 0) {
@@ -1013,7 +1019,8 @@ bool plan_smem(DecodeArgs &p, int G, int optin, size_t *smem_out) {
   const uint64_t logit_bytes = align16((uint64_t)T * E * 4);
   const uint64_t cand_bytes = (uint64_t)T * 8 * 8 * 8;  // top-k candidates: T x 8 groups x 8 (key, id)
   const uint64_t misc_bytes = align16(4ull * (5 * A + rows + 2 + 8));  // ids w srt skey segb active + 8 scalars
-  const uint64_t small = 32ull * 8 + y_bytes + logit_bytes + cand_bytes + misc_bytes;
+  // (+ 1 KB: the kernel's static e8m0 table comes out of the same per-block budget)
+  const uint64_t small = 32ull * 8 + y_bytes + logit_bytes + cand_bytes + misc_bytes + 1024;
   const uint64_t budget = (uint64_t)optin - 1024;
   auto stages = [&](uint64_t tail) { return tail >= budget ? 0 : std::min<int>(4, (int)((budget - tail) / p.stage_bytes)); };
   // Q8(h) in the region of Q8(x) (both outside the ring), or in the last
@@ -1154,7 +1161,8 @@ moe_status decode_forward(const char *name, const void *x, moe_dtype x_dtype, in
           (!sh || ((uintptr_t)sh->sg % 16 == 0 && (uintptr_t)sh->su % 16 == 0));
   p.d16 = nbI % 16 == 0 && (uintptr_t)sd % 16 == 0 && (!sh || (uintptr_t)sh->sd % 16 == 0);
 
-  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), optin - 1024, name);
+  // the dynamic limit leaves room for the static shared memory (the e8m0 table and a few words)
+  const moe_status ast = ensure_smem_attr(reinterpret_cast<const void *>(kern), optin - 2048, name);
   if (ast != MOE_OK) return ast;
   if (clear_ws) {  // every check has passed: only now is anything enqueued
     err = cudaMemsetAsync(workspace, 0, moe_decode_workspace_bytes(), static_cast<cudaStream_t>(stream));

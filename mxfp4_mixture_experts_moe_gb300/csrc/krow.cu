@@ -86,7 +86,7 @@ MOE_DEVFN int pn_block(const uint4 &lo, const uint4 &hi, const uint4 &w) {
 // xrow, then the block scales) or in global memory (xg, sg).
 template <int NM, int S, bool STAGED>
 MOE_DEVFN void krow_dot(uint32_t xrow, const int8_t *xg, const float *sg, int K, const uint32_t (&wrow)[NM],
-                        const uint32_t (&srow)[NM], float (&acc)[NM]) {
+                        const uint32_t (&srow)[NM], uint32_t tab, float (&acc)[NM]) {
   const int lane = threadIdx.x & 31;
   const int nb = K / 32;
 #pragma unroll
@@ -109,7 +109,7 @@ MOE_DEVFN void krow_dot(uint32_t xrow, const int8_t *xg, const float *sg, int K,
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
         const int I = pn_block(lo, hi, lds128(wrow[m] + 16u * b));
-        acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, e8m0_half(lds_u8(srow[m] + b))), acc[m]);
+        acc[m] = __fmaf_rn(__int2float_rn(I), __fmul_rn(sx, lds_f32(tab + 4u * lds_u8(srow[m] + b))), acc[m]);
       }
     }
   }
@@ -137,12 +137,14 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
   // (it % NS, it % kGroups), phase it / lcm(NS, kGroups).
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NS * p.stage_bytes);
   uint64_t *empty = full + NS * kGroups;
+  const uint32_t stab = smem_addr(empty + NS);  // [256] e8m0_half table
   const int L = NS % kGroups == 0 ? NS : NS % 2 == 0 ? 2 * NS : kGroups * NS;  // lcm(NS, kGroups = 4)
-  int *active = reinterpret_cast<int *>(empty + NS);  // [E]
+  int *active = reinterpret_cast<int *>(empty + NS) + 256;  // [E]
   int *offs = active + p.E;                           // [E+1]
   float *ys = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(offs + p.E + 1) + 15) & ~uintptr_t(15));  // [A][R] (CMB)
 
   for (int i = tid; i <= p.E; i += blockDim.x) offs[i] = p.offsets[i];
+  fill_e8m0_table(stab);
   if (tid == 0) {
     for (int s = 0; s < NS * kGroups; ++s) mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx + 32 cp.async arrives
     for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&empty[s]), kGroupWarps);
@@ -282,9 +284,9 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
           if (!resolve(q, a, arow)) continue;
           float acc[2];
           if (q - seg_b < p.armax)
-            krow_dot<2, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, acc);
+            krow_dot<2, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, stab, acc);
           else
-            krow_dot<2, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, acc);
+            krow_dot<2, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, stab, acc);
           float y0, y1;
           reduce_pair(acc[0], acc[1], y0, y1);
           if (lane == 0) {
@@ -303,9 +305,9 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
           if (!resolve(q, a, arow)) continue;
           float acc[2];
           if (q - seg_b < p.armax)
-            krow_dot<2, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, acc);
+            krow_dot<2, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, stab, acc);
           else
-            krow_dot<2, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, acc);
+            krow_dot<2, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, stab, acc);
           float g, u;
           reduce_pair(acc[0], acc[1], g, u);
           if (lane == 0) {
@@ -382,7 +384,7 @@ moe_status launch_krow(int mode, const int8_t *aq, int64_t ld_aq, const float *a
   p.s16 = (nb % 16) == 0 && (uintptr_t)s0 % 16 == 0 && (s1 == nullptr || (uintptr_t)s1 % 16 == 0);
   p.as16 = (uintptr_t)as % 16 == 0 && ld_as % 4 == 0;
   const bool cmb = mode == kKDown && cout != nullptr;
-  const size_t fixed = (kGroups + 1) * 8 * kKrowMaxStages + 4 * (size_t)(2 * E + 1) + 16 +
+  const size_t fixed = (kGroups + 1) * 8 * kKrowMaxStages + 1024 + 4 * (size_t)(2 * E + 1) + 16 +
                        (cmb ? (size_t)p.A * p.R * 4 + 16 : 0) + 64;
   const size_t budget = (size_t)optin - 1024;
   if (budget < fixed) return fail(MOE_ERR_UNSUPPORTED, "%s: no shared-memory plan", name);

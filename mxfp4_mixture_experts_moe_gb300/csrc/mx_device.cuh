@@ -456,14 +456,24 @@ MOE_DEVFN void row_dot_global(const int8_t *xr, const float *sr, int K, const ui
   }
 }
 
+// The 256 values e8m0_half(u) as a table in shared memory (1 KB at tab), so
+// that the hot loops turn a scale byte into its factor with one load instead
+// of the integer decode.  The block's threads write the entries; the caller
+// synchronises before the first use.
+MOE_DEVFN void fill_e8m0_table(uint32_t tab) {
+  for (uint32_t u = threadIdx.x; u < 256u; u += blockDim.x) sts32(tab + 4u * u, __float_as_uint(e8m0_half(u)));
+}
+
 // NM weight rows read block by block from shared memory (not preloaded into
 // registers) against one staged activation row: the form for weights that
 // are used by one activation row only.  wrow[m] / srow[m]: shared addresses of
-// row m's packed codes and scale bytes.  Same terms, same order per lane as
-// row_dot_smem_pn.
-template <int NM, int S>
+// row m's packed codes and scale bytes; tab: the e8m0_half table (TAB), or
+// unused (the scale bytes decoded in registers, for instantiations where the
+// table's extra loads would cost register spills).  Same terms, same order
+// per lane as row_dot_smem_pn.
+template <int NM, int S, bool TAB = true>
 MOE_DEVFN void row_dot_stage_pn(uint32_t xrow, int K, const uint32_t (&wrow)[NM], const uint32_t (&srow)[NM],
-                                float (&acc)[NM]) {
+                                uint32_t tab, float (&acc)[NM]) {
   const int lane = threadIdx.x & 31;
   const int nb = K / 32;
 #pragma unroll
@@ -478,7 +488,8 @@ MOE_DEVFN void row_dot_stage_pn(uint32_t xrow, int K, const uint32_t (&wrow)[NM]
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
         const uint4 w = lds128(wrow[m] + 16u * b);
-        const float ws = e8m0_half(lds_u8(srow[m] + b));
+        const uint32_t u = lds_u8(srow[m] + b);
+        const float ws = TAB ? lds_f32(tab + 4u * u) : e8m0_half(u);
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
         int dp = 0, dn = 0;
 #pragma unroll

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   uint8_t *stages = smem;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)nstage * p.stage_bytes);
   uint64_t *empty = full + nstage;
-  int *active = reinterpret_cast<int *>(empty + nstage);  // [E] active experts, in id order
+  const uint32_t stab = smem_addr(empty + nstage);        // [256] e8m0_half table
+  int *active = reinterpret_cast<int *>(empty + nstage) + 256;  // [E] active experts, in id order
   int *offs = active + p.E;                               // [E+1] copy of offsets
   int *rowtab = offs + p.E + 1;                           // [cap] activation row per sorted position
   uint8_t *act = reinterpret_cast<uint8_t *>(rowtab + (p.rowtab ? p.cap : 0));
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
   // Stage the expert offsets in one parallel pass, then list the experts
   // that own rows (ballot compaction keeps increasing id order).
   for (int i = tid; i <= p.E; i += blockDim.x) offs[i] = p.offsets[i];
+  fill_e8m0_table(stab);
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(smem_addr(&full[s]), 33);  // 1 expect_tx arrive + 32 cp.async arrives
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(512, 1) mx_expert_kernel(const MxArgs p) {
             const uint32_t wrow[2] = {sbase + (uint32_t)r * (p.K / 2), sbase + p.wreg + (uint32_t)r * (p.K / 2)};
             const uint32_t srow[2] = {sbase + 2 * p.wreg + (uint32_t)r * nb, sbase + 2 * p.wreg + p.sreg + (uint32_t)r * nb};
             float acc[2];
-            row_dot_stage_pn<2, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wrow, srow, acc);
+            row_dot_stage_pn<2, S>(act_base + (uint32_t)arow * p.act_row_bytes, p.K, wrow, srow, stab, acc);
             float g, u;
             reduce_pair(acc[0], acc[1], g, u);
             if (lane == 0) put_gateup(a, r, g, u);
@@ -510,7 +512,7 @@ moe_status launch_mx(MxArgs p, cudaStream_t stream, const char *name) {
   const int sms = sm_count();
   p.rowtab = p.cap <= kRowTab ? 1 : 0;
   p.act_row_bytes = (uint32_t)p.K + 8u * nb;
-  const size_t fixed = (size_t)p.E * 8 + 4 + 16 * 8 + 32 + (p.rowtab ? 4 * (size_t)p.cap : 0) + 16;
+  const size_t fixed = (size_t)p.E * 8 + 4 + 16 * 8 + 32 + 1024 + (p.rowtab ? 4 * (size_t)p.cap : 0) + 16;
   int G = p.N < sms ? p.N : sms;
   for (;;) {
     p.R = (p.N + G - 1) / G;
