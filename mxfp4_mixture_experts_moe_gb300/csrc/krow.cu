@@ -276,26 +276,36 @@ __global__ void __launch_bounds__(kKrowThreads, 1) krow_kernel(const KrowArgs p)
     const uint32_t sbase = smem_addr(stages + (size_t)st * p.stage_bytes);
     const uint32_t abase = sbase + p.act_off;
     if constexpr (MODE == kKDown) {
-      // two output rows per warp, u and u + nu (each keeps its own arithmetic)
-      const int nu = (nrow + 1) >> 1;
+      // four output rows per warp, u + j nu (j < 4; each keeps its own
+      // arithmetic, the activation loads serve all four); a row past the
+      // slice repeats row u and is not written
+      const int nu = (nrow + 3) >> 2;
       for (int u = wig; u < nu; u += kGroupWarps) {
-        const int v2 = u + nu < nrow ? u + nu : u;
-        const uint32_t wrow[2] = {sbase + (uint32_t)u * (K / 2), sbase + (uint32_t)v2 * (K / 2)};
-        const uint32_t srow[2] = {sbase + p.wreg + (uint32_t)u * nb, sbase + p.wreg + (uint32_t)v2 * nb};
+        int rr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rr[j] = u + j * nu < nrow ? u + j * nu : u;
+        uint32_t wrow[4], srow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          wrow[j] = sbase + (uint32_t)rr[j] * (K / 2);
+          srow[j] = sbase + p.wreg + (uint32_t)rr[j] * nb;
+        }
 #pragma unroll 1
         for (int q = seg_b; q < seg_e; ++q) {
           int a, arow;
           if (!resolve(q, a, arow)) continue;
-          float acc[2];
+          float acc[4];
           if (q - seg_b < p.armax)
-            krow_dot<2, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, stab, acc);
+            krow_dot<4, S, true>(abase + (uint32_t)(q - seg_b) * p.act_row, nullptr, nullptr, K, wrow, srow, stab, acc);
           else
-            krow_dot<2, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, stab, acc);
-          float y0, y1;
-          reduce_pair(acc[0], acc[1], y0, y1);
+            krow_dot<4, S, false>(0, p.aq + (int64_t)arow * p.ld_aq, p.as + (int64_t)arow * p.ld_as, K, wrow, srow, stab, acc);
+          float y[4];
+          reduce_pair(acc[0], acc[1], y[0], y[1]);
+          reduce_pair(acc[2], acc[3], y[2], y[3]);
           if (lane == 0) {
-            put_down(a, r0 + u, y0);
-            if (v2 != u) put_down(a, r0 + v2, y1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j == 0 || rr[j] != u) put_down(a, r0 + rr[j], y[j]);
           }
         }
       }
