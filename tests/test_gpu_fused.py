@@ -64,6 +64,19 @@ def test_fused_equals_stage_calls(moe, dsv4, T):
     assert moe.moe_device_status() == 0
 
 
+def test_fused_one_token_sweep(moe, dsv4):
+    """Many one-token calls, each against the stage calls bit for bit.  The
+    two consumer groups of the single launch share its three ring stages, so
+    this also checks that no group reads a stage before its own item landed
+    (a parity wait that met a barrier one phase behind gave wrong h rows in a
+    few calls of a sweep like this one)."""
+    x = synth.activations(synth.DSV4, 24, token0=900)
+    for t in range(x.shape[0]):
+        xt = dev(x[t:t + 1])
+        _same(_forward(moe, dsv4, xt, True), _forward(moe, dsv4, xt, False))
+    assert moe.moe_device_status() == 0
+
+
 def test_fused_tiny_layer_and_padding(moe):
     spec = synth.TINY  # I = 128 < 152 SMs: some CTAs own no gate/up rows
     lw = upload_layer(spec)
